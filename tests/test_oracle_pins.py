@@ -1,0 +1,324 @@
+"""Pins for the CPU oracle: facts the pages print, closed forms and brute force.
+
+None of these tests re-types the oracle's formulas.  The gather is checked
+against an independent formulation (numpy strided views, zero padding and
+slicing); the swizzle against the page's identity case, a typed chunk table,
+per-mode chunk rules and brute-force bijection; the store against numpy slice
+assignment and guard bytes; the tile enumeration against the positions the
+CuTe-DSL page prints.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FACTS = json.load(open(os.path.join(GOLDEN, "page_facts.json")))
+
+
+# --------------------------------------------------------------------------
+# independent helpers (numpy array semantics, no oracle code)
+# --------------------------------------------------------------------------
+def np_view(buf: np.ndarray, v: oracle.View) -> np.ndarray:
+    """Element view of ``buf`` as an array shaped outermost-first + (esize,) bytes."""
+    shape = tuple(int(d) for d in reversed(v.dims)) + (v.esize,)
+    strides = tuple(int(s) for s in reversed(v.strides)) + (1,)
+    return np.lib.stride_tricks.as_strided(buf, shape=shape, strides=strides, writeable=True)
+
+
+def np_box(buf: np.ndarray, v: oracle.View, origin) -> np.ndarray:
+    """The box at ``origin`` (innermost first) with zero bytes outside the tensor.
+
+    Built by zero-padding every dimension by the box extent and slicing.
+    """
+    a = np_view(buf, v)
+    c = [int(x) for x in reversed(origin)]
+    b = [int(x) for x in reversed(v.box)]
+    n = [int(x) for x in reversed(v.dims)]
+    pads = [(max(0, -ci), max(0, ci + bi - ni)) for ci, bi, ni in zip(c, b, n)]
+    p = np.pad(a, pads + [(0, 0)])
+    sl = tuple(slice(ci + lo, ci + lo + bi) for ci, bi, (lo, _) in zip(c, b, pads))
+    return p[sl]  # shape outermost-first box + (esize,)
+
+
+def chunk_permutation(box_bytes: int, mode: str) -> np.ndarray:
+    """dest_offset[src_offset] built from 16-byte chunk rules per 128-byte line.
+
+    NONE keeps every chunk; 32B/64B/128B XOR the chunk number inside each
+    128-byte line with the line number modulo 2/4/8 (the swizzle span divided
+    by 16 bytes).  Written with integer division and modulo over lines and
+    chunks, not with bit masks.
+    """
+    period_lines = {"none": 1, "32B": 2, "64B": 4, "128B": 8}[mode]
+    span_chunks = period_lines  # chunks that can move: 2, 4 or 8 of the 8 per line
+    dest = np.empty(box_bytes, dtype=np.int64)
+    for o in range(box_bytes):
+        line, within = divmod(o, 128)
+        chunk, byte = divmod(within, 16)
+        group, low = divmod(chunk, span_chunks)
+        low = low ^ (line % period_lines)
+        dest[o] = line * 128 + (group * span_chunks + low) * 16 + byte
+    return dest
+
+
+def swizzle_image(unswizzled: np.ndarray, mode: str) -> np.ndarray:
+    dest = chunk_permutation(unswizzled.size, mode)
+    out = np.empty_like(unswizzled)
+    out[dest] = unswizzled
+    return out
+
+
+# --------------------------------------------------------------------------
+# page facts
+# --------------------------------------------------------------------------
+def test_single_tile_is_16384_bytes():
+    f = FACTS["single_tile_fp32"]
+    v = oracle.View(4, (64, 64), (4, 256), (64, 64))
+    assert oracle.box_bytes(v) == f["box_bytes"] == 16384
+    assert oracle.box_bytes(oracle.View(*_c(datagen.C1))) == 16384
+
+
+def test_cute_dsl_payload_and_smem_request():
+    f = FACTS["cute_dsl_fp16_strips"]
+    v = oracle.View(*_c(datagen.C2))
+    assert oracle.box_bytes(v) == f["payload_bytes"] == 32768
+    # the allocation is payload plus one 8-byte barrier; the expected
+    # transaction count is the payload alone
+    assert oracle.box_bytes(v) + f["barrier_bytes"] == f["smem_request_bytes"]
+
+
+def test_cute_dsl_924_tiles_and_block1_iter2():
+    f = FACTS["cute_dsl_fp16_strips"]
+    v = oracle.View(*_c(datagen.C2))
+    assert oracle.grid_count(v) == f["tile_loads"] == f["blocks"] * f["tiles_per_block"]
+    coords = oracle.grid_coords(v)
+    # block b owns row strip b and walks j = 0..6: tile index b*7 + j
+    t = f["example_block"] * f["tiles_per_block"] + f["example_iteration"]
+    x, y = coords[t]
+    assert (y, x) == tuple(f["example_element_origin_row_col"])
+    # load that tile from matrices whose elements hold their own row (resp.
+    # column) index and read which rows and columns it actually covers
+    rows, cols = 8448, 1792
+    row_of = np.ascontiguousarray(np.broadcast_to(np.arange(rows, dtype=np.uint16)[:, None], (rows, cols)))
+    col_of = np.ascontiguousarray(np.broadcast_to(np.arange(cols, dtype=np.uint16)[None, :], (rows, cols)))
+    for val, (lo, hi) in ((row_of, f["example_rows"]), (col_of, f["example_cols"])):
+        img = oracle.tile_load(v, val.view(np.uint8).ravel(), coords[t:t + 1])
+        got = img.view(np.uint16).reshape(64, 256)
+        assert got.min() == lo and got.max() == hi
+
+
+def test_identity_swizzle_leaves_offsets_unchanged():
+    f = FACTS["cute_dsl_identity_swizzle"]
+    assert f["bits"] == 0
+    for o in range(0, 1 << 16):
+        assert oracle.swizzle(o, "none") == o
+
+
+def test_swizzle128_matches_chunk_table():
+    rows = [list(map(int, ln.split())) for ln in open(os.path.join(GOLDEN, "swizzle128_chunk_table.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 8
+    for rep in range(3):  # pattern repeats every 1024 bytes
+        for r in range(8):
+            for c in range(8):
+                for b in (0, 7, 15):
+                    src = rep * 1024 + r * 128 + c * 16 + b
+                    dst = rep * 1024 + r * 128 + rows[r][c] * 16 + b
+                    assert oracle.swizzle(src, "128B") == dst
+
+
+@pytest.mark.parametrize("mode", ["none", "32B", "64B", "128B"])
+def test_swizzle_chunk_rules(mode):
+    n = 4096
+    dest = chunk_permutation(n, mode)
+    got = np.array([oracle.swizzle(o, mode) for o in range(n)])
+    np.testing.assert_array_equal(got, dest)
+
+
+@pytest.mark.parametrize("mode", ["none", "32B", "64B", "128B"])
+@pytest.mark.parametrize("box_bytes", [128, 1024, 4096, 8192, 16384, 32768])
+def test_swizzle_is_bijection_on_box(mode, box_bytes):
+    img = np.array([oracle.swizzle(o, mode) for o in range(box_bytes)])
+    assert img.min() == 0 and img.max() == box_bytes - 1
+    assert np.unique(img).size == box_bytes
+
+
+def test_swizzle_keeps_16_byte_chunks_and_lines():
+    for mode in ("32B", "64B", "128B"):
+        for o in range(0, 8192, 3):
+            s = oracle.swizzle(o, mode)
+            assert s % 16 == o % 16          # bytes inside a chunk stay in order
+            assert s // 128 == o // 128      # a chunk never leaves its 128-byte line
+
+
+# --------------------------------------------------------------------------
+# gather / store vs an independent numpy formulation
+# --------------------------------------------------------------------------
+def _c(w: datagen.Workload):
+    return (w.esize, w.dims, w.strides, w.box, w.swizzle)
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4, 8])
+def test_gather_brute_force_small_2d(esize):
+    rows, cols = 5, 7
+    v = oracle.View(esize, (cols, rows), (esize, cols * esize), (4, 4))
+    buf = datagen.random_bytes(rows * cols * esize, 11 + esize)
+    origins = np.array([(x, y) for y in range(-4, 9) for x in range(-4, 9)], dtype=np.int32)
+    packed = oracle.tile_load(v, buf, origins)
+    bb = oracle.box_bytes(v)
+    for i, o in enumerate(origins):
+        want = np_box(buf, v, o).reshape(-1)
+        np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], want, err_msg=f"origin {o}")
+
+
+@pytest.mark.parametrize("mode", ["32B", "64B", "128B"])
+def test_gather_swizzled_small(mode):
+    span = {"32B": 32, "64B": 64, "128B": 128}[mode]
+    esize = 2
+    inner = span // esize
+    rows, cols = 37, inner * 3 - 5  # ragged in both directions
+    v = oracle.View(esize, (cols, rows), (esize, cols * esize + 16), (inner, 16), mode)
+    buf = datagen.random_bytes(v.span_bytes() + 64, 21)
+    origins = np.array([(x, y) for y in (-15, -1, 0, 5, 21, 36) for x in (-inner, -8, 0, 8, cols - 8, cols)],
+                       dtype=np.int32)
+    packed = oracle.tile_load(v, buf, origins)
+    bb = oracle.box_bytes(v)
+    for i, o in enumerate(origins):
+        want = swizzle_image(np_box(buf, v, o).reshape(-1), mode)
+        np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], want, err_msg=f"origin {o}")
+
+
+def test_gather_permuted_3d_view():
+    # storage [6, 3, 8] fp32 contiguous, view = permute(1, 0, 2): shape [3, 6, 8]
+    S = datagen.random_bytes(6 * 3 * 8 * 4, 31)
+    v = oracle.View(4, (8, 6, 3), (4, 3 * 8 * 4, 8 * 4), (4, 4, 2), "none")
+    arr = S.view(np.uint32).reshape(6, 3, 8).transpose(1, 0, 2)  # numpy's own permute
+    g = datagen.rng(5)
+    origins = np.stack([g.integers(-3, 8, 200), g.integers(-3, 6, 200), g.integers(-1, 3, 200)], 1).astype(np.int32)
+    packed = oracle.tile_load(v, S, origins).view(np.uint32)
+    for i, (x, y, z) in enumerate(origins):
+        want = np.zeros((2, 4, 4), dtype=np.uint32)
+        for kz in range(2):
+            for ky in range(4):
+                for kx in range(4):
+                    zz, yy, xx = z + kz, y + ky, x + kx
+                    if 0 <= zz < 3 and 0 <= yy < 6 and 0 <= xx < 8:
+                        want[kz, ky, kx] = arr[zz, yy, xx]
+        np.testing.assert_array_equal(packed[i * 32:(i + 1) * 32], want.ravel())
+
+
+@pytest.mark.parametrize("rank", [1, 2, 3, 4, 5])
+def test_gather_each_rank(rank):
+    dims = (9, 4, 3, 2, 3)[:rank]
+    box = (4, 3, 2, 2, 2)[:rank]
+    esize = 2
+    strides = [esize]
+    for d in range(1, rank):
+        strides.append(strides[-1] * dims[d - 1] + (16 if d == 1 else 0))
+    v = oracle.View(esize, dims, tuple(strides), box)
+    buf = datagen.random_bytes(v.span_bytes() + 32, 40 + rank)
+    g = datagen.rng(rank)
+    origins = np.stack([g.integers(-b + 1, n, 64) for n, b in zip(dims, box)], 1).astype(np.int32)
+    packed = oracle.tile_load(v, buf, origins)
+    bb = oracle.box_bytes(v)
+    for i, o in enumerate(origins):
+        np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], np_box(buf, v, o).reshape(-1))
+
+
+def test_store_matches_slice_assignment_and_keeps_guard_bytes():
+    rows, cols, esize = 11, 13, 4
+    pitch = cols * esize + 12  # 12 guard bytes after every row
+    v = oracle.View(esize, (cols, rows), (esize, pitch), (8, 4))
+    fill = 0xA5
+    base = np.full(pitch * rows + 64, fill, dtype=np.uint8)
+    origins = np.array([(x, y) for y in (-3, 0, 4, 8, 10) for x in (-7, 0, 5, 8, 12)], dtype=np.int32)
+    packed = datagen.random_bytes(len(origins) * oracle.box_bytes(v), 51)
+    oracle.tile_store(v, base, origins, packed)
+    # independent: numpy slice assignment, in list order, clipped to the tensor
+    want = np.full_like(base, fill)
+    a = np_view(want, v)
+    bb = oracle.box_bytes(v)
+    for i, (x, y) in enumerate(origins):
+        img = packed[i * bb:(i + 1) * bb].reshape(4, 8, esize)
+        y0, y1 = max(y, 0), min(y + 4, rows)
+        x0, x1 = max(x, 0), min(x + 8, cols)
+        if y0 < y1 and x0 < x1:
+            a[y0:y1, x0:x1] = img[y0 - y:y1 - y, x0 - x:x1 - x]
+    np.testing.assert_array_equal(base, want)
+    # guard bytes between rows and after the tensor never change
+    for r in range(rows):
+        assert (base[r * pitch + cols * esize:(r + 1) * pitch] == fill).all()
+    assert (base[rows * pitch:] == fill).all()
+
+
+@pytest.mark.parametrize("mode", ["none", "128B"])
+def test_store_after_load_is_identity(mode):
+    rows, cols, esize = 300, 200, 2
+    box = (64, 32) if mode == "128B" else (40, 24)
+    v = oracle.View(esize, (cols, rows), (esize, cols * esize), box, mode)
+    src = datagen.random_bytes(rows * cols * esize, 61)
+    coords = oracle.grid_coords(v)
+    packed = oracle.tile_load(v, src, coords)
+    dst = np.zeros_like(src)
+    oracle.tile_store(v, dst, coords, packed)
+    np.testing.assert_array_equal(dst, src)
+    dst2 = np.full_like(src, 7)
+    oracle.roundtrip(v, src, v, dst2, coords)
+    np.testing.assert_array_equal(dst2, src)
+
+
+def test_c3_edge_tiles_zero_counts():
+    w = datagen.C3
+    v = oracle.View(*_c(w))
+    assert oracle.grid_count(v) == 79 * 47 == 3713
+    coords = oracle.grid_coords(v)
+    # nonzero storage so that every zero byte in an image is fill
+    buf = (datagen.random_bytes(w.storage_bytes, 3) | np.uint8(1))
+    bb = oracle.box_bytes(v)
+    last_row = np.nonzero(coords[:, 1] == 78 * 128)[0]
+    last_col = np.nonzero(coords[:, 0] == 46 * 64)[0]
+    corner = np.intersect1d(last_row, last_col)
+    assert len(last_row) == 47 and len(last_col) == 79 and len(corner) == 1
+    packed = oracle.tile_load(v, buf, coords[[0, last_row[0], last_col[0], corner[0]]])
+    zeros = [(packed[i * bb:(i + 1) * bb] == 0).sum() for i in range(4)]
+    valid_rows, valid_cols = 10000 - 78 * 128, 3000 - 46 * 64
+    assert (valid_rows, valid_cols) == (16, 56)
+    assert zeros[0] == 0
+    assert zeros[1] == (128 - valid_rows) * 64 * 2
+    assert zeros[2] == 128 * (64 - valid_cols) * 2
+    assert zeros[3] == (128 * 64 - valid_rows * valid_cols) * 2
+
+
+def test_c4_random_origins_touch_tensor_and_are_aligned():
+    w = datagen.C4
+    c = datagen.workload_coords(w)
+    assert c.shape == (4096, 3)
+    assert (c[:, 0] % 4 == 0).all()  # 16-byte granularity along the contiguous dimension
+    for d in range(3):
+        assert (c[:, d] + w.box[d] - 1 >= 0).all() and (c[:, d] < w.dims[d]).all()
+    partial = ((c[:, 0] < 0) | (c[:, 0] + 32 > 1024) | (c[:, 1] < 0) | (c[:, 1] + 64 > 512)).mean()
+    assert 0.15 < partial < 0.4
+
+
+def test_day76_sixteen_tiles():
+    f = FACTS["day76_matrix"]
+    v = oracle.View(4, (256, 256), (4, 1024), (64, 64))
+    assert oracle.grid_count(v) == f["tiles"]
+    coords = oracle.grid_coords(v)
+    # coordinates are innermost first: tile (blockIdx.x, blockIdx.y) -> (64 bx, 64 by)
+    assert [tuple(c) for c in coords[:5]] == [(0, 0), (64, 0), (128, 0), (192, 0), (0, 64)]
+
+
+def test_swapped_coordinates_load_transposed_positions():
+    # swapping x and y fetches the mirror tile: a whole tile of wrong values
+    v = oracle.View(4, (256, 256), (4, 1024), (64, 64))
+    buf = datagen.random_bytes(256 * 256 * 4, 77)
+    right = oracle.tile_load(v, buf, np.array([[64, 128]], dtype=np.int32))
+    swapped = oracle.tile_load(v, buf, np.array([[128, 64]], dtype=np.int32))
+    assert (right.view(np.uint32) != swapped.view(np.uint32)).mean() > 0.99
+    a = buf.view(np.uint32).reshape(256, 256)
+    np.testing.assert_array_equal(right.view(np.uint32).reshape(64, 64), a[128:192, 64:128])
