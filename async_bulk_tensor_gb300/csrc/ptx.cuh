@@ -1,0 +1,232 @@
+// Hand-written PTX for the async proxy on sm_103a: mbarriers with transaction
+// counts, tensor-map (TMA) and 1-D bulk copies, bulk async groups, proxy
+// fences.  Nothing here depends on libcu++ so that every wait can be bounded.
+//
+// Instruction forms follow the pages' description of the mechanism:
+//   "lesson 04: TMA - the async bulk copy engine", sections "Load completion -
+//   the mbarrier and the byte budget", "Store completion - commit group and
+//   wait group" and "The real toolchain - PTX and the descriptor object";
+//   "Day 76: The Tensor Memory Accelerator (TMA)", "Hint 2" (fence, store,
+//   commit, wait_group.read) and "Pitfalls" (fence after barrier init).
+#pragma once
+
+#include <cstdint>
+
+namespace atb {
+namespace ptx {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier --------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t arrivals)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(arrivals) : "memory");
+}
+
+// Makes barrier initialisation visible to the async proxy (the engine's
+// complete_tx updates) and to the rest of the CTA after the block barrier.
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy engine) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One arrival plus a byte budget for the current phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// True once the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- tensor-map copies -----------------------------------------------------
+__device__ __forceinline__ void prefetch_tensor_map(const void* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Global -> shared box load, completion counted in bytes on `bar`.
+template <int R>
+__device__ __forceinline__ void tma_load(uint32_t dst, const void* map, const int32_t* c, uint32_t bar);
+
+template <>
+__device__ __forceinline__ void tma_load<1>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2}], [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(bar)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load<2>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(bar)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load<3>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(bar)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load<4>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(bar)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load<5>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]),
+        "r"(bar)
+        : "memory");
+}
+
+// Shared -> global box store, completion tracked by the bulk async group.
+template <int R>
+__device__ __forceinline__ void tma_store(const void* map, const int32_t* c, uint32_t src);
+
+template <>
+__device__ __forceinline__ void tma_store<1>(const void* map, const int32_t* c, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.1d.global.shared::cta.tile.bulk_group [%0, {%1}], [%2];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0]), "r"(src)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store<2>(const void* map, const int32_t* c, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0]), "r"(c[1]), "r"(src)
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store<3>(const void* map, const int32_t* c, uint32_t src)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(src)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store<4>(const void* map, const int32_t* c, uint32_t src)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(src)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store<5>(const void* map, const int32_t* c, uint32_t src)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(src)
+        : "memory");
+}
+
+// ---- 1-D bulk copies (contiguous byte ranges, 16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// ---- bulk async groups -----------------------------------------------------
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N committed groups still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Runtime-depth variant (0..7); larger values clamp to 7.
+__device__ __forceinline__ void bulk_wait_read_le(uint32_t n)
+{
+    switch (n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    case 6: bulk_wait_read<6>(); break;
+    default: bulk_wait_read<7>(); break;
+    }
+}
+
+// Wait until every committed group has fully completed (writes included).
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+}  // namespace ptx
+}  // namespace atb

@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark: TMA tiled round trip of a 16384x16384 fp16 tensor (512 MiB) on GB300.
+
+One step = one pass of the whole hot path over the workload: every 64x256 box
+of the source is loaded by the tensor-map engine into a shared-memory stage
+(arrive.expect_tx + cp.async.bulk.tensor) and stored to the destination
+(cp.async.bulk.tensor store + bulk group), i.e. one atb_tile_roundtrip launch.
+The maps are encoded once per tensor, outside the device-timed region.
+
+Prints ONE JSON line (rank 0):
+  value      HBM GB/s moved (bytes read + bytes written) / device time, inputs
+             resident in HBM, timed with CUDA events on the launching stream
+  e2e        the same metric through the public call with HOST buffers:
+             pinned H2D of the input, encode, round trip, D2H of the output
+  roofline   the round-trip kernel against the measured copy bandwidth
+  cpu_baseline  the plain CPU oracle on the host cores (single thread)
+  sweep / ablations  stage sweep and the thread-issued copies beside it
+
+``--impl reference`` times the oracle instead (the reference arm).
+Inputs (512 MiB in + 512 MiB out) exceed the 129 MB L2, so no flush is needed.
+Multi-GPU (torchrun): every rank moves its own full replica; no collective on
+the data path; value = bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "tile_pipeline_roundtrip_f16_16384.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "async_bulk_tensor_gb300", "csrc", f) for f in ("pipeline.cu", "ptx.cuh")]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only; the data path has no collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def init_dist(world_size: int, backend: str):
+    import torch.distributed as dist
+
+    if world_size > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world_size > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(dist, local_seconds: float, local_units: float, device=None):
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    seconds = max_over_ranks(dist, local_seconds, device)
+    units = local_units
+    if dist is not None:
+        import torch
+
+        t = torch.tensor([local_units], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        units = float(t.item())
+    return units, seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str, period_ms: int = 100):
+        self.proc = None
+        self.cmd = ["nvidia-smi", f"--query-gpu={','.join(CLOCK_FIELDS)}", "--format=csv,noheader,nounits",
+                    "-lms", str(period_ms), "-i", str(gpu_id)]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        mhz, max_mhz, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < len(CLOCK_FIELDS):
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                max_mhz = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max_mhz,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# peaks and the committed ncu traffic figure
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """(bytes per full-workload launch, note) from the committed ncu summary, or
+    (None, why) when it is missing or the kernel source changed since."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None, "no committed ncu summary"
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not m or not h:
+        return None, "summary lacks traffic or source hash"
+    if h.group(1) != kernel_source_hash():
+        return None, "kernel changed since the ncu capture"
+    return int(m.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum, scaled per launch"
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def time_launches(torch, stream, fn, steps: int, warmup: int, dist=None, device=None) -> float:
+    """Seconds for `steps` calls of fn() on `stream` (CUDA events), after warm-up."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    stream.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            fn()
+        end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    barrier(dist)
+    return start.elapsed_time(end) / 1e3
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import async_bulk_tensor_gb300 as atb
+    import datagen
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = init_dist(world, "nccl")
+    atb.init_device()
+    atb.device_status()
+    stream = torch.cuda.Stream(device=device)
+
+    w = datagen.C5A if args.box == "64x256" else datagen.C5B
+    launch = dict(stages=args.stages, ctas_per_sm=args.ctas_per_sm)
+    src_h = datagen.storage(w)
+    nbytes = w.storage_bytes
+    src = torch.from_numpy(src_h).to(device)
+    dst = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+    ms = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle)
+    md = atb.encode_tiled(w.dtype, dst, w.dims, w.strides, w.box, w.swizzle)
+    tiles = atb.grid_tiles(ms)
+    bytes_per_step = 2 * nbytes  # every element read once and written once (all boxes in bounds)
+
+    def step():
+        atb.tile_roundtrip(ms, md, stream=stream, **launch)
+
+    # correctness of the timed configuration before timing it
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    atb.check_device(stream)
+    verified = bool(torch.equal(src, dst))
+    if not verified:
+        raise SystemExit("round trip output differs from its input; refusing to time it")
+    dst.zero_()
+
+    visible = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    gpu_id = visible[local_rank] if local_rank < len(visible) else str(local_rank)
+    with ClockSampler(gpu_id) as clocks:
+        seconds = time_launches(torch, stream, step, args.steps, args.warmup, dist, device)
+    atb.check_device(stream)
+    units, max_seconds = aggregate(dist, seconds, float(bytes_per_step) * args.steps, device)
+    value = units / max_seconds / 1e9
+    ms_per_step = max_seconds / args.steps * 1e3
+    kernel_avg_s = seconds / args.steps  # one launch per step: the launch's own duration
+    achieved = bytes_per_step / kernel_avg_s / 1e9
+
+    result = {"metric": "TMA tiled round trip HBM GB/s (read+write)", "value": round(value, 1), "unit": "GB/s",
+              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+              "data": "synthetic (seeded normal(0,1) fp16)"}
+    result["config"] = {
+        "workload": w.name, "tensor": "16384x16384 fp16 row-major (512 MiB)",
+        "box": args.box, "swizzle": w.swizzle, "tiles_per_step": tiles, "stages": args.stages or 4,
+        "ctas_per_sm": args.ctas_per_sm or "auto", "parallelism": f"replicas x{world}",
+        "l2": "inputs larger than L2 (512 MiB read + 512 MiB written per step); no flush",
+    }
+    result["tiles_per_s"] = round(tiles * args.steps * world / max_seconds, 1)
+    peak, peak_kind = hbm_peak()
+    traffic, traffic_note = committed_traffic()
+    result["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                          "peak_source": f"{peak_kind} hbm_gbs (copy, read+write)",
+                          "traffic_note": traffic_note, "frac_of_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4)}
+    result["gpu_launches"] = args.steps
+    result["clocks"] = clocks.summary()
+
+    if rank == 0 and not args.no_extras:
+        result["sweep"] = stage_sweep(torch, atb, datagen, device, stream, src, dst, args)
+        result["ablations"] = ablations(torch, atb, device, stream, src, dst, nbytes, args)
+        atb.check_device(stream)
+    if not args.no_e2e:
+        result["e2e"] = end_to_end(torch, atb, w, device, stream, src_h, nbytes, bytes_per_step, args, dist)
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(w, src_h)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
+    out = {}
+    steps = max(50, min(400, args.steps // 10))
+    for w, box in ((datagen.C5A, "64x256"), (datagen.C5B, "128x64_sw128")):
+        ms = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle)
+        md = atb.encode_tiled(w.dtype, dst, w.dims, w.strides, w.box, w.swizzle)
+        for stages in (2, 4, 6, 8):
+            key = f"{box}_s{stages}"
+            try:
+                atb.pipeline_smem_bytes(ms, stages)
+            except atb.AtbError as e:
+                out[key] = f"infeasible: {e.name}"
+                continue
+            s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, stages=stages),
+                              steps, 5)
+            out[key] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
+    return out
+
+
+def ablations(torch, atb, device, stream, src, dst, nbytes, args):
+    steps = max(50, min(400, args.steps // 10))
+    res = {}
+    for name, fn in (("cpasync_ldgsts", atb.copy_cpasync), ("ldst_global_v4", atb.copy_ldst_v4),
+                     ("cudaMemcpyAsync_d2d", atb.copy_memcpy)):
+        s = time_launches(torch, stream, lambda: fn(src, dst, nbytes, stream=stream), steps, 5)
+        res[name] = round(2 * nbytes * steps / s / 1e9, 1)
+    return res
+
+
+def end_to_end(torch, atb, w, device, stream, src_h, nbytes, bytes_per_step, args, dist):
+    """Through the public call with host buffers: pinned H2D, encode, round trip, D2H."""
+    src_pin = torch.from_numpy(src_h).pin_memory()
+    out_pin = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    src = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def step():
+        src.copy_(src_pin, non_blocking=True)
+        ms = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle)
+        md = atb.encode_tiled(w.dtype, dst, w.dims, w.strides, w.box, w.swizzle)
+        atb.tile_roundtrip(ms, md, stream=stream, stages=args.stages, ctas_per_sm=args.ctas_per_sm)
+        out_pin.copy_(dst, non_blocking=True)
+
+    steps = max(3, args.e2e_steps)
+    seconds = time_launches(torch, stream, step, steps, 3, dist, device)
+    atb.check_device(stream)
+    ok = bool((out_pin[:1 << 20] == src_pin[:1 << 20]).all()) and bool(torch.equal(out_pin[-(1 << 20):],
+                                                                                      src_pin[-(1 << 20):]))
+    units, max_s = aggregate(dist, seconds, float(bytes_per_step) * steps, device)
+    return {"value": round(units / max_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "steps": steps, "ms_per_step": round(max_s / steps * 1e3, 3),
+            "verified_sample": ok}
+
+
+def cpu_baseline(w, src_h):
+    """The oracle as it stands, single-threaded, on one full round trip of the workload."""
+    import numpy as np
+
+    import oracle
+
+    v = oracle.View(w.esize, w.dims, w.strides, w.box, w.swizzle)
+    coords = oracle.grid_coords(v)
+    dst = np.zeros_like(src_h)
+    t0 = time.perf_counter()
+    oracle.roundtrip(v, src_h, v, dst, coords)
+    dt = time.perf_counter() - t0
+    return {"value": round(2 * w.storage_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one full round trip of {w.name} ({len(coords)} boxes, 1 GiB moved), "
+                      f"single thread, {dt:.2f} s; host has {os.cpu_count()} cores",
+            "matches_input": bool(np.array_equal(dst, src_h))}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import numpy as np
+
+    import datagen
+    import oracle
+
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = datagen.C5A if args.box == "64x256" else datagen.C5B
+    v = oracle.View(w.esize, w.dims, w.strides, w.box, w.swizzle)
+    coords = oracle.grid_coords(v)
+    sample_tiles = args.ref_tiles
+    sample = coords[:sample_tiles]
+    src_h = datagen.storage(w)
+    dst = np.zeros_like(src_h)
+    bytes_per_step = 2 * len(sample) * oracle.box_bytes(v)
+    for _ in range(args.warmup):
+        oracle.roundtrip(v, src_h, v, dst, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.roundtrip(v, src_h, v, dst, sample)
+    dt = time.perf_counter() - t0
+    value = bytes_per_step * args.steps / dt / 1e9
+    desc = (f"first {len(sample)} of {len(coords)} boxes of {w.name} per step "
+            f"({bytes_per_step / 2**20:.0f} MiB moved), single thread")
+    print(json.dumps({
+        "impl": "reference", "metric": "TMA tiled round trip HBM GB/s (read+write)", "value": round(value, 4),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded normal(0,1) fp16)",
+        "config": {"workload": w.name, "box": args.box, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=8000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["atb", "reference"], default="atb")
+    p.add_argument("--box", choices=["64x256", "128x64"], default="64x256")
+    p.add_argument("--stages", type=int, default=0, help="0 = library default")
+    p.add_argument("--ctas-per-sm", type=int, default=0, help="0 = library default")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--ref-tiles", type=int, default=1024, help="boxes per reference-arm step")
+    p.add_argument("--no-extras", action="store_true", help="skip the stage sweep and ablations")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

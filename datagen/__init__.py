@@ -18,7 +18,8 @@ Recipes follow the workloads the pages describe:
     out-of-bounds boxes, and a 512 MiB fp16 bandwidth case, which exercise the
     descriptor rules and zero fill described in "GPU TMA tensor memory
     accelerator", "The architecture: every piece explained".
-All values are seeded (numpy PCG64); nothing is read from disk.
+All values are seeded (numpy PCG64, or torch's CPU generator for the normal draws);
+nothing is read from disk.
 """
 from __future__ import annotations
 
@@ -116,8 +117,12 @@ def rng(seed: int) -> np.random.Generator:
 
 
 def random_bytes(nbytes: int, seed: int) -> np.ndarray:
-    """Uniform random byte patterns (every bit pattern possible, NaNs included)."""
-    return np.frombuffer(rng(seed).bytes(nbytes), dtype=np.uint8).copy()
+    """Uniform random byte patterns (every bit pattern possible, NaNs included).
+
+    Raw 64-bit PCG64 outputs, viewed as little-endian bytes.
+    """
+    words = rng(seed).bit_generator.random_raw((nbytes + 7) // 8)
+    return words.view(np.uint8)[:nbytes].copy()
 
 
 def uniform_bf16_bytes(n_elems: int, seed: int) -> np.ndarray:
@@ -130,9 +135,12 @@ def uniform_bf16_bytes(n_elems: int, seed: int) -> np.ndarray:
 
 
 def normal_f16_bytes(n_elems: int, seed: int) -> np.ndarray:
-    """normal(0, 1) drawn in fp32 and converted to fp16."""
-    x = rng(seed).standard_normal(n_elems, dtype=np.float32).astype(np.float16)
-    return x.view(np.uint8)
+    """normal(0, 1) drawn in fp32 by torch's seeded CPU generator, rounded to fp16."""
+    import torch
+
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n_elems, generator=g, dtype=torch.float32).to(torch.float16)
+    return x.view(torch.uint8).numpy()
 
 
 def storage(w: Workload, seed: int | None = None) -> np.ndarray:

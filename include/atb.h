@@ -1,0 +1,321 @@
+/*
+ * atb.h -- C ABI of libatb, tiled tensor movement between HBM and shared
+ * memory through the Tensor Memory Accelerator (TMA), for sm_103a (GB300).
+ *
+ * Sources the operations follow (web pages on the TMA):
+ *   [L04]  "lesson 04: TMA - the async bulk copy engine"
+ *   [ARC]  "GPU TMA tensor memory accelerator"
+ *   [D76]  "Day 76: The Tensor Memory Accelerator (TMA)"
+ *   [CDSL] "Understanding TMA loads in CuTe DSL"
+ *
+ * Conventions shared by every call
+ *   - Coordinates, extents and box sizes are listed innermost (contiguous)
+ *     dimension first: x, then y, ... ([D76] "Pitfalls", coordinates in the
+ *     wrong order).  Coordinates are element offsets (int32) of a box's first
+ *     element and may be negative or past the end: a load reads zero bytes
+ *     there, a store drops those elements.
+ *   - Along the innermost dimension a box origin must sit on a 16-byte
+ *     boundary: x * element_size must be a multiple of 16.  Kernels check it
+ *     per box; a violating box is skipped and ATB_ERR_COORD_ALIGN is recorded
+ *     in the device status (see atb_device_status).
+ *   - A "packed" buffer holds n box images back to back, image i at byte
+ *     offset i * box_bytes, each byte-for-byte the shared-memory image of that
+ *     box as the engine writes it (swizzle applied, stage base aligned to the
+ *     swizzle period).  It must be 16-byte aligned.
+ *   - Device pointers are plain CUDA device addresses owned by the caller.
+ *     The library allocates device memory only once per device, lazily, for a
+ *     small status block (see atb_device_status); call atb_init_device() before
+ *     capturing any of these calls into a CUDA graph.
+ *   - All launches are asynchronous on the caller's stream (NULL = the legacy
+ *     default stream).  Host-detectable errors return before anything is
+ *     launched; atb_last_error() then holds a sentence naming the rule, the
+ *     dimension and the value.
+ *   - Errors raised inside a kernel (a wait that ran out of time, a misaligned
+ *     box origin) are recorded in the device status block and reported by
+ *     atb_device_status(); the kernel returns early instead of hanging.
+ *   - Not thread-safe across host threads for atb_last_error(), which is
+ *     thread-local; every other call may be used from any thread.
+ */
+#ifndef ATB_H
+#define ATB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATB_VERSION 1
+#define ATB_MAX_RANK 5
+
+/* A CUDA stream handle; layout-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* atb_stream_t;
+
+typedef enum {
+    ATB_OK = 0,
+    ATB_ERR_RANK = 1,            /* rank outside 1..5 */
+    ATB_ERR_BOX_DIM = 2,         /* a box extent is 0 or above 256 */
+    ATB_ERR_STRIDE_ALIGN = 3,    /* a byte stride (dims 1..rank-1) is not a multiple of 16 */
+    ATB_ERR_BASE_ALIGN = 4,      /* global base address not 16-byte aligned */
+    ATB_ERR_SMEM_ALIGN = 5,      /* packed buffer not 16-byte aligned */
+    ATB_ERR_SWIZZLE = 6,         /* unknown swizzle mode */
+    ATB_ERR_SWIZZLE_SPAN = 7,    /* swizzled box: inner box bytes differ from the swizzle span */
+    ATB_ERR_INNER_BYTES = 8,     /* inner box bytes not a multiple of 16 */
+    ATB_ERR_DTYPE = 9,           /* unknown element type */
+    ATB_ERR_DRIVER = 10,         /* the driver's encoder is unavailable or refused the map */
+    ATB_ERR_UNSUPPORTED_DEVICE = 11, /* current device is not compute capability 10.3 */
+    ATB_ERR_SMEM_BUDGET = 12,    /* stages x stage bytes exceed the per-block shared memory */
+    ATB_ERR_ARG = 13,            /* a null pointer, zero extent, bad stride or mismatched maps */
+    ATB_ERR_TIMEOUT = 14,        /* (device) an mbarrier wait ran out of time */
+    ATB_ERR_CUDA = 15,           /* a CUDA runtime call failed */
+    ATB_ERR_COORD_ALIGN = 16,    /* (device) a box origin breaks the 16-byte rule along x */
+    ATB_ERR_COORD_RANGE = 17,    /* (device) a box origin is beyond +-2^30 */
+    ATB_ERR_STRIDE_RANGE = 18,   /* a byte stride (dims 1..rank-1) is 0 or not below 2^40 */
+    ATB_ERR_DIM_RANGE = 19       /* an extent is 0 or above 2^32 */
+} atb_status;
+
+typedef enum {
+    ATB_U8 = 0, ATB_U16 = 1, ATB_U32 = 2, ATB_I32 = 3, ATB_U64 = 4, ATB_I64 = 5,
+    ATB_F16 = 6, ATB_F32 = 7, ATB_F64 = 8, ATB_BF16 = 9
+} atb_dtype;
+
+typedef enum {
+    ATB_SWIZZLE_NONE = 0, ATB_SWIZZLE_32B = 1, ATB_SWIZZLE_64B = 2, ATB_SWIZZLE_128B = 3
+} atb_swizzle;
+
+typedef enum {
+    ATB_L2_PROMO_NONE = 0, ATB_L2_PROMO_64B = 1, ATB_L2_PROMO_128B = 2, ATB_L2_PROMO_256B = 3
+} atb_l2_promotion;
+
+typedef enum {
+    ATB_OOB_ZERO = 0             /* out-of-bounds load elements read as zero bytes */
+} atb_oob_fill;
+
+/*
+ * An encoded tensor map plus the parameters it was built from.  `map` is the
+ * driver's 128-byte CUtensorMap ([D76] "The address arithmetic moves into a
+ * descriptor": 128 opaque bytes); the rest is kept for validation, launch
+ * sizing and the ragged-store path.  Treat it as read-only; it may be copied
+ * by value, and must outlive the calls that use it (the kernels receive a copy
+ * by value, so it may be freed once the call has returned).
+ */
+typedef struct {
+    unsigned char map[128];
+    uint64_t base;                    /* global address the map was encoded over */
+    uint64_t dims[ATB_MAX_RANK];      /* innermost first */
+    uint64_t strides[ATB_MAX_RANK];   /* byte strides; strides[0] = element size */
+    uint32_t box[ATB_MAX_RANK];       /* innermost first */
+    uint32_t rank;
+    uint32_t esize;                   /* element size in bytes */
+    uint32_t dtype;                   /* atb_dtype */
+    uint32_t swizzle;                 /* atb_swizzle */
+    uint32_t l2_promotion;            /* atb_l2_promotion */
+    uint32_t oob_fill;                /* atb_oob_fill */
+    uint32_t box_bytes;               /* product of box extents x element size */
+    uint32_t magic;                   /* set by atb_encode_tiled */
+} atb_tensor_map;
+
+/* Pipeline shape of one launch.  Zero fields take the library defaults. */
+typedef struct {
+    uint32_t stages;       /* shared-memory ring depth, 1..16 (default 4) */
+    uint32_t ctas;         /* total CTAs; 0 = persistent grid of ctas_per_sm per SM */
+    uint32_t ctas_per_sm;  /* 0 = as many as shared memory allows, at most 2 */
+    uint32_t schedule;     /* 0 = box t goes to CTA t mod G; 1 = CTA b takes a contiguous run */
+    uint32_t store_groups; /* bulk-store groups allowed in flight at once, 1..8, clamped to
+                              `stages` (0 = min(stages, 8)); a stage is recycled as soon as
+                              the group that stores from it has finished reading it */
+    uint32_t reserved[3];
+} atb_launch;
+
+/* Contents of the device status block (one per device). */
+typedef struct {
+    int32_t code;          /* atb_status of the first device-side error, 0 = none */
+    int32_t block;         /* CTA that recorded it */
+    int32_t tile;          /* box index (position in the list or grid) it was working on */
+    int32_t where;         /* 1 producer wait, 2 consumer wait, 3 producer issue, 4 consumer issue,
+                              5 self-test wait */
+    uint32_t errors;       /* number of device-side errors recorded since the last reset */
+    uint32_t reserved[3];
+} atb_device_report;
+
+/* Library version (ATB_VERSION). */
+int atb_version(void);
+
+/* sizeof(atb_tensor_map), so bindings can check their mirror of the struct. */
+size_t atb_tensor_map_size(void);
+
+/* Human-readable name of a status code.  Static storage; never NULL. */
+const char* atb_status_string(atb_status s);
+
+/* The last host-side error of this thread, as a sentence ("" if none). */
+const char* atb_last_error(void);
+
+/*
+ * atb_encode_tiled -- build and validate a tiled tensor map.
+ *
+ * [D76] "The address arithmetic moves into a descriptor" and "Pitfalls"
+ * (the encoder returns a bare invalid-value error for any broken rule),
+ * [L04] "The real toolchain - PTX and the descriptor object" (the map is
+ * encoded once on the host and handed to the kernel as a grid constant),
+ * [ARC] "The architecture: every piece explained" (shape, strides, box and
+ * out-of-bounds fill live in the descriptor).
+ *
+ * Checks, each with its own status before the driver is asked:
+ *   rank in 1..5                                 -> ATB_ERR_RANK
+ *   dtype known                                  -> ATB_ERR_DTYPE
+ *   gbase non-null and 16-byte aligned           -> ATB_ERR_ARG / ATB_ERR_BASE_ALIGN
+ *   every dims[d] in 1..2^32                     -> ATB_ERR_DIM_RANGE
+ *   strides_bytes[d] (d = 1..rank-1) multiple of 16 -> ATB_ERR_STRIDE_ALIGN
+ *   strides_bytes[d] in 16..2^40-16               -> ATB_ERR_STRIDE_RANGE
+ *   (strides need not grow with d: permuted views are passed as they are)
+ *   every box[d] in 1..256                       -> ATB_ERR_BOX_DIM
+ *   box[0] * element size multiple of 16         -> ATB_ERR_INNER_BYTES
+ *   swizzle known                                -> ATB_ERR_SWIZZLE
+ *   swizzled: box[0] * element size == span (32/64/128) -> ATB_ERR_SWIZZLE_SPAN
+ *   elem_strides NULL or all 1                   -> ATB_ERR_ARG
+ * then fetches cuTensorMapEncodeTiled through the runtime's driver entry point
+ * (no libcuda link) and encodes; a driver refusal -> ATB_ERR_DRIVER.
+ *
+ *   out           caller-owned result (any alignment)
+ *   gbase         device address of element (0, ..., 0)
+ *   dims          rank extents, innermost first
+ *   strides_bytes rank entries: strides_bytes[0] is ignored (the innermost
+ *                 dimension is contiguous), strides_bytes[d] is the byte
+ *                 distance between neighbours along dimension d; NULL is not
+ *                 allowed for rank > 1
+ *   box           rank box extents, innermost first
+ *   elem_strides  NULL, or rank entries that must all be 1
+ */
+atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank, void* gbase,
+                            const uint64_t* dims, const uint64_t* strides_bytes,
+                            const uint32_t* box, const uint32_t* elem_strides,
+                            atb_swizzle swizzle, atb_l2_promotion l2_promotion,
+                            atb_oob_fill oob_fill);
+
+/* Box bytes of a map (product of the box extents x element size); 0 if map is NULL. */
+size_t atb_box_bytes(const atb_tensor_map* map);
+
+/* Number of boxes that tile the whole tensor, edge boxes included; 0 if map is NULL. */
+uint64_t atb_grid_tiles(const atb_tensor_map* map);
+
+/*
+ * Dynamic shared memory one CTA of a pipeline with `stages` stages over this
+ * map needs (stage ring, barriers, alignment slack), in *bytes.
+ * ATB_ERR_SMEM_BUDGET if it exceeds the device's per-block limit (the
+ * requested value is still written).
+ */
+atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, size_t* bytes);
+
+/*
+ * atb_tile_load -- gather boxes into a packed buffer of shared-memory images.
+ *
+ * [L04] "What the issuing thread actually does" and "Load completion - the
+ * mbarrier and the byte budget"; [D76] "An exact round trip"; [CDSL] "Issue
+ * the load and wait for its phase".  A persistent, warp-specialised CTA ring:
+ * one producer thread arms stage s with arrive.expect_tx(box_bytes) and issues
+ * one cp.async.bulk.tensor per box; one consumer thread waits on the stage's
+ * phase and drains the landed image with a 1-D bulk store to
+ * d_packed + i * box_bytes, recycling the stage after the bulk group's reads.
+ *
+ *   src       encoded map of the source tensor
+ *   d_coords  device array of n * rank int32 origins, innermost first; NULL =
+ *             every box of the tile grid in row-major tile order (innermost
+ *             tile index fastest), n is then ignored
+ *   d_packed  device output, 16-byte aligned, n * box_bytes bytes
+ *   launch    NULL for defaults
+ * n = 0 launches nothing.
+ */
+atb_status atb_tile_load(const atb_tensor_map* src, const int32_t* d_coords, uint64_t n,
+                         void* d_packed, const atb_launch* launch, atb_stream_t stream);
+
+/*
+ * atb_tile_store -- write packed box images back into a tensor.
+ *
+ * [L04] "Store completion - commit group and wait group"; [D76] "Exercise",
+ * "Hint 2" and "Solution" (the shared-to-global direction, completed through
+ * a bulk async group, not an mbarrier).  The producer brings image i into a
+ * stage with a 1-D bulk copy counted by the stage's mbarrier; the consumer
+ * issues the tensor store, commits it and recycles the stage after
+ * wait_group.read.  Elements outside the tensor are not written.  A box whose
+ * origin is negative in any dimension is written by the consumer warp with
+ * plain clipped stores instead (a tensor store may not start before the
+ * tensor), and so is a box that crosses the end of a row whose byte length
+ * (dims[0] x element size) is not a multiple of 16: the engine writes the
+ * last 16-byte chunk of such a row whole, which would spill past the row.
+ * Boxes that overlap with different contents land in an unspecified order.
+ *
+ *   dst       encoded map of the destination tensor
+ *   d_coords  as for atb_tile_load (NULL = tile grid)
+ *   d_packed  device input, 16-byte aligned, n * box_bytes bytes
+ */
+atb_status atb_tile_store(const atb_tensor_map* dst, const int32_t* d_coords, uint64_t n,
+                          const void* d_packed, const atb_launch* launch, atb_stream_t stream);
+
+/*
+ * atb_tile_roundtrip -- move boxes from one tensor to another through shared
+ * memory: load with the source map, store with the destination map.
+ *
+ * [D76] "Exercise" (a second map over the output; the only global traffic is
+ * two bulk tensor instructions), [L04] "Why this only pays off inside a
+ * pipeline" and [ARC] "The architecture" / "End-to-end flow" (an N-stage ring,
+ * stage k mod N, a stage refilled only after its consumer is done).
+ * Result = store(dst, coords, load(src, coords)).
+ *
+ *   src, dst  maps with equal rank, element size, box extents and swizzle
+ *             (ATB_ERR_ARG otherwise); extents and strides may differ.
+ *             Source and destination memory must not overlap.
+ *   d_coords  as for atb_tile_load (NULL = the source's tile grid)
+ */
+atb_status atb_tile_roundtrip(const atb_tensor_map* src, const atb_tensor_map* dst,
+                              const int32_t* d_coords, uint64_t n, const atb_launch* launch,
+                              atb_stream_t stream);
+
+/*
+ * Allocate this device's status block now (it is otherwise allocated on the
+ * first launch on the device).  Call before capturing launches in a graph.
+ */
+atb_status atb_init_device(void);
+
+/*
+ * Synchronise `stream`, copy the current device's status block into *report
+ * (may be NULL) and reset it.  Returns the recorded code (ATB_OK if none).
+ */
+atb_status atb_device_status(atb_stream_t stream, atb_device_report* report);
+
+/* Limit for every mbarrier wait inside the kernels, in nanoseconds of the
+ * GPU's global timer (default 1e9 = one second).  0 restores the default. */
+void atb_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Self-test of the bounded wait: one CTA waits on an mbarrier that nothing
+ * will complete, gives up after timeout_ns, records ATB_ERR_TIMEOUT (where =
+ * 5) in the status block and returns.  No copy is in flight.  Returns the
+ * launch status; read the outcome with atb_device_status().
+ */
+atb_status atb_selftest_wait_timeout(uint64_t timeout_ns, atb_stream_t stream);
+
+/*
+ * Bandwidth ablations (flat copies of `bytes` bytes, both pointers 16-byte
+ * aligned, bytes a multiple of 16):
+ *   atb_copy_cpasync  thread-issued cp.async (LDGSTS, 16 B per lane) into a
+ *                     shared-memory ring, then ld.shared.v4 / st.global.v4
+ *                     ([L04] "What the issuing thread actually does": the
+ *                     Ampere-style copy where every lane issues its slice);
+ *   atb_copy_ldst_v4  plain coalesced ld.global.v4 / st.global.v4 through
+ *                     registers ([D76] the per-thread loads of the diagram in
+ *                     "The address arithmetic moves into a descriptor");
+ *   atb_copy_memcpy   cudaMemcpyAsync device-to-device.
+ * `launch` may be NULL; only `ctas`, `ctas_per_sm` and `stages` are used.
+ */
+atb_status atb_copy_cpasync(const void* d_src, void* d_dst, size_t bytes, const atb_launch* launch,
+                            atb_stream_t stream);
+atb_status atb_copy_ldst_v4(const void* d_src, void* d_dst, size_t bytes, const atb_launch* launch,
+                            atb_stream_t stream);
+atb_status atb_copy_memcpy(const void* d_src, void* d_dst, size_t bytes, atb_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATB_H */

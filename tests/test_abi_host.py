@@ -1,0 +1,102 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/atb.h declares, agrees with the binding on struct layouts, and the
+encoder rejects each broken rule with its own status before the driver is
+asked ("Day 76: The Tensor Memory Accelerator (TMA)", "Pitfalls": the driver
+alone answers every broken rule with one invalid-value code)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "atb.h")
+
+
+@pytest.fixture(scope="module")
+def atb():
+    import async_bulk_tensor_gb300 as atb
+
+    return atb
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(atb_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("atb_encode_tiled", "atb_tile_load", "atb_tile_store", "atb_tile_roundtrip",
+                     "atb_device_status", "atb_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(atb):
+    out = subprocess.run(["nm", "-D", "--defined-only", atb.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\bT\s+(atb_\w+)", out.stdout))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        getattr(atb.lib, n)
+
+
+def test_struct_layouts(atb):
+    assert atb.lib.atb_tensor_map_size() == ctypes.sizeof(atb.TensorMap)
+    assert ctypes.sizeof(atb.Launch) == 32
+    assert ctypes.sizeof(atb.DeviceReport) == 32
+
+
+def test_status_strings(atb):
+    for i, name in enumerate(atb.STATUS):
+        assert atb.status_string(i) == name
+
+
+def _expect(atb, code, **kw):
+    args = dict(dtype="f16", base=0x10000, dims=(1024, 64), strides_bytes=(2, 2048), box=(64, 16))
+    args.update(kw)
+    with pytest.raises(atb.AtbError) as e:
+        atb.encode_tiled(**args)
+    assert e.value.code == code, str(e.value)
+    return str(e.value)
+
+
+def test_encoder_rules_each_have_their_own_status(atb):
+    _expect(atb, atb.ATB_ERR_RANK, dims=(2,) * 6, strides_bytes=(2,) + (16,) * 5, box=(8,) * 6)
+    _expect(atb, atb.ATB_ERR_RANK, dims=(), strides_bytes=(), box=())
+    _expect(atb, atb.ATB_ERR_DTYPE, dtype=42)
+    _expect(atb, atb.ATB_ERR_ARG, base=0)
+    assert "0x10008" in _expect(atb, atb.ATB_ERR_BASE_ALIGN, base=0x10008)
+    _expect(atb, atb.ATB_ERR_DIM_RANGE, dims=(1024, 0))
+    _expect(atb, atb.ATB_ERR_DIM_RANGE, dims=((1 << 32) + 1, 4))
+    msg = _expect(atb, atb.ATB_ERR_STRIDE_ALIGN, strides_bytes=(2, 2040))
+    assert "strides_bytes[1]" in msg and "2040" in msg
+    _expect(atb, atb.ATB_ERR_STRIDE_RANGE, strides_bytes=(2, 1 << 40))
+    msg = _expect(atb, atb.ATB_ERR_BOX_DIM, box=(64, 257))
+    assert "box[1]" in msg
+    _expect(atb, atb.ATB_ERR_BOX_DIM, box=(0, 16))
+    _expect(atb, atb.ATB_ERR_INNER_BYTES, box=(12, 16))  # 24 bytes
+    _expect(atb, atb.ATB_ERR_SWIZZLE, swizzle=9)
+    _expect(atb, atb.ATB_ERR_SWIZZLE_SPAN, box=(32, 16), swizzle="128B")  # 64 bytes != 128
+    _expect(atb, atb.ATB_ERR_SWIZZLE_SPAN, box=(64, 16), swizzle="32B")
+    _expect(atb, atb.ATB_ERR_ARG, elem_strides=(1, 2))
+
+
+def test_valid_map_reaches_the_driver(atb):
+    # With no GPU driver the entry point is unavailable; on a GPU the map encodes.
+    try:
+        m = atb.encode_tiled("f16", 0x10000, (1024, 64), (2, 2048), (64, 16))
+    except atb.AtbError as e:
+        assert e.code == atb.ATB_ERR_DRIVER
+    else:
+        assert atb.box_bytes(m) == 64 * 16 * 2
+
+
+def test_null_maps_are_rejected_without_a_device(atb):
+    m = atb.TensorMap()  # never encoded
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_roundtrip(m, m)
+    assert e.value.code == atb.ATB_ERR_ARG
+    assert atb.box_bytes(m) == 0 and atb.grid_tiles(m) == 0
