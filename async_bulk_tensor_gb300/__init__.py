@@ -116,6 +116,7 @@ def _load():
         "atb_device_status": (S, [P, ctypes.POINTER(DeviceReport)]),
         "atb_set_wait_timeout_ns": (None, [U64]),
         "atb_selftest_wait_timeout": (S, [U64, P]),
+        "atb_tile_roundtrip_noalloc": (S, [MapP, MapP, P, U64, LaunchP, P, ctypes.POINTER(DeviceReport)]),
         "atb_copy_cpasync": (S, [P, P, SZ, LaunchP, P]),
         "atb_copy_ldst_v4": (S, [P, P, SZ, LaunchP, P]),
         "atb_copy_memcpy": (S, [P, P, SZ, P]),
@@ -221,6 +222,23 @@ def tile_roundtrip(src: TensorMap, dst: TensorMap, coords=None, n: int = 0, stre
     """``atb_tile_roundtrip``: store(dst, coords, load(src, coords)); ``coords=None`` = tile grid."""
     _check(lib.atb_tile_roundtrip(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
                                   ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_roundtrip")
+
+
+def tile_roundtrip_noalloc(src: TensorMap, dst: TensorMap, coords=None, n: int = 0, stream=None,
+                           report: bool = True, **launch) -> DeviceReport | None:
+    """``atb_tile_roundtrip_noalloc``: the round trip without any device allocation.
+
+    With ``report=True`` the call waits for the stream and returns the kernel's
+    error record (a non-OK record is returned, not raised); with ``report=False``
+    it returns None right after the launch.
+    """
+    rep = DeviceReport() if report else None
+    code = lib.atb_tile_roundtrip_noalloc(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
+                                          ctypes.byref(_launch(**launch)), _stream(stream),
+                                          ctypes.byref(rep) if rep is not None else None)
+    if rep is None or code != rep.code:
+        _check(code, "atb_tile_roundtrip_noalloc")
+    return rep
 
 
 def init_device():

@@ -419,9 +419,12 @@ atb_status prepare_kernel(KernelFn fn, const DeviceInfo& dev)
     return ATB_OK;
 }
 
+// `caller_status`, when given, receives the kernel's error record instead of
+// the device's lazily allocated status block.
 template <int MODE>
 atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst, const int32_t* coords, uint64_t n,
-                           void* packed, const atb_launch* cfg, cudaStream_t stream)
+                           void* packed, const atb_launch* cfg, cudaStream_t stream,
+                           DeviceStatus* caller_status = nullptr)
 {
     clear_error();
     const atb_tensor_map* shape = MODE == kStore ? dst : src;
@@ -465,9 +468,11 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
                          stages, stage_bytes_for(shape), smem, dev.smem_optin);
     if (n_tiles == 0) return ATB_OK;
 
-    DeviceStatus* status = nullptr;
-    st = device_status_block(&status);
-    if (st != ATB_OK) return st;
+    DeviceStatus* status = caller_status;
+    if (!status) {
+        st = device_status_block(&status);
+        if (st != ATB_OK) return st;
+    }
 
     KernelFn fn = kernel_for_rank<MODE>(rank);
     st = prepare_kernel(fn, dev);
@@ -524,12 +529,70 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     return ATB_OK;
 }
 
+// ---- allocation-free round trip ---------------------------------------------
+// Scratch of atb_tile_roundtrip_noalloc: the kernel's error record lives in
+// this file-scope device array instead of a block obtained from cudaMalloc.
+// The module loader reserves it on every GPU that loads the library, and it
+// stays reserved until the process exits.  All calls on one device share it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATB_NOALLOC_SCRATCH_BYTES];
+static_assert(sizeof(DeviceStatus) <= ATB_NOALLOC_SCRATCH_BYTES, "status record must fit the static scratch");
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[64];
+
+// Device address of the array on the current device.  In host code the
+// array's name stands for a host-side shadow, never for device memory, so the
+// address must come from the runtime, once per device, with that device current.
+atb_status noalloc_scratch_address(const DeviceInfo& dev, void** out)
+{
+    if (dev.device < 0 || dev.device >= 64) return set_error(ATB_ERR_ARG, "device ordinal %d out of range", dev.device);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_address[dev.device]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(no-allocation scratch)");
+        if (!p) return set_error(ATB_ERR_CUDA, "cudaGetSymbolAddress returned a null scratch address");
+        g_noalloc_address[dev.device] = p;
+    }
+    *out = g_noalloc_address[dev.device];
+    return ATB_OK;
+}
+
 }  // namespace
 }  // namespace atb
 
 using namespace atb;
 
 extern "C" {
+
+atb_status atb_tile_roundtrip_noalloc(const atb_tensor_map* src, const atb_tensor_map* dst, const int32_t* d_coords,
+                                      uint64_t n, const atb_launch* launch, atb_stream_t stream,
+                                      atb_device_report* report)
+{
+    clear_error();
+    DeviceInfo dev;
+    atb_status st = current_device(&dev);
+    if (st != ATB_OK) return st;
+    const size_t needed = sizeof(DeviceStatus);  // this kernel's scratch does not grow with the problem
+    if (needed > ATB_NOALLOC_SCRATCH_BYTES)
+        return set_error(ATB_ERR_ARG, "the round trip needs %zu bytes of scratch; the static array holds %d",
+                         needed, ATB_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    st = noalloc_scratch_address(dev, &scratch);
+    if (st != ATB_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's record: start this one from zero.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, needed, s);
+    if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync(no-allocation scratch)");
+    st = launch_pipeline<kRoundtrip>(src, dst, d_coords, n, nullptr, launch, s, static_cast<DeviceStatus*>(scratch));
+    if (st != ATB_OK) return st;
+    if (!report) return ATB_OK;
+    e = cudaMemcpyAsync(report, scratch, needed, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_error(e, "cudaMemcpyAsync(no-allocation report)");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "cudaStreamSynchronize");
+    return static_cast<atb_status>(report->code);
+}
 
 atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, size_t* bytes)
 {

@@ -296,6 +296,43 @@ void atb_set_wait_timeout_ns(uint64_t ns);
 atb_status atb_selftest_wait_timeout(uint64_t timeout_ns, atb_stream_t stream);
 
 /*
+ * atb_tile_roundtrip_noalloc -- atb_tile_roundtrip for callers that must not
+ * allocate device memory.  The pages have no counterpart to this call.
+ *
+ * atb_tile_roundtrip records kernel errors in a status block that the library
+ * obtains with cudaMalloc the first time it runs on a device.  Some callers
+ * cannot let that happen: code being captured into a CUDA graph in global
+ * capture mode (where cudaMalloc is refused), services that reserve all of a
+ * GPU's memory for their own pool at start-up and forbid any later
+ * allocation, and latency-critical threads that must not take the driver's
+ * allocation path.  This entry point moves the same boxes with the same kernel
+ * but keeps the error record in a static device array of
+ * ATB_NOALLOC_SCRATCH_BYTES bytes that is part of the library image: every GPU
+ * that loads the library holds those bytes until the process exits.  It calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *   src, dst, d_coords, n, launch, stream  as for atb_tile_roundtrip
+ *   report  NULL: return right after the launch (kernel errors are then not
+ *           reported).  Otherwise host memory: the call waits for `stream`,
+ *           copies the error record there and returns its code.
+ *
+ * Scratch: this kernel needs sizeof(atb_device_report) bytes whatever the
+ * problem size; a call that would need more than ATB_NOALLOC_SCRATCH_BYTES is
+ * rejected with ATB_ERR_ARG before anything is launched.  Every call on a
+ * device shares the one array, which keeps the last call's record; each call
+ * clears it (an asynchronous memset on `stream`) before its launch.  Calls
+ * whose work overlaps on the GPU (different streams, or a second call issued
+ * before the first one's report was read) race on that record.
+ * The first call on each device looks up the array's device address (one
+ * runtime query, with that device current); make that first call before any
+ * stream capture begins.
+ */
+#define ATB_NOALLOC_SCRATCH_BYTES 256
+atb_status atb_tile_roundtrip_noalloc(const atb_tensor_map* src, const atb_tensor_map* dst,
+                                      const int32_t* d_coords, uint64_t n, const atb_launch* launch,
+                                      atb_stream_t stream, atb_device_report* report);
+
+/*
  * Bandwidth ablations (flat copies of `bytes` bytes, both pointers 16-byte
  * aligned, bytes a multiple of 16):
  *   atb_copy_cpasync  thread-issued cp.async (LDGSTS, 16 B per lane) into a
