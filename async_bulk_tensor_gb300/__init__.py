@@ -73,7 +73,9 @@ class Launch(ctypes.Structure):
         ("ctas_per_sm", ctypes.c_uint32),
         ("schedule", ctypes.c_uint32),
         ("store_groups", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32 * 3),
+        ("l2_hints", ctypes.c_uint32),
+        ("no_pdl", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
     ]
 
 
@@ -159,9 +161,12 @@ def _check(code: int, where: str):
         raise AtbError(code, where, lib.atb_last_error().decode(errors="replace"))
 
 
-def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0) -> Launch:
+HINT_LOAD_EVICT_FIRST, HINT_STORE_EVICT_FIRST, HINT_STORE_EVICT_LAST = 1, 2, 4
+
+
+def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True) -> Launch:
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
-                  store_groups)
+                  store_groups, l2_hints, 0 if pdl else 1)
 
 
 def version() -> int:

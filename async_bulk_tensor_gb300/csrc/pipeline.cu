@@ -61,6 +61,7 @@ struct PipeArgs {
     uint32_t contiguous;    // 1: CTA b takes a contiguous run of boxes
     uint32_t swizzle_bits;  // 0 none, 1 32B, 2 64B, 3 128B
     uint32_t dst_ragged_x;  // destination rows end inside a 16-byte chunk
+    uint32_t l2_hints;      // ATB_HINT_* bits
 };
 
 // Shared-memory control words after the stage ring and the barriers.
@@ -246,13 +247,20 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
         if (MODE != kStore) ptx::prefetch_tensor_map(&src_map);
         if (MODE != kLoad) ptx::prefetch_tensor_map(&dst_map);
     }
+    // Let the next launch on the stream be scheduled now; it sets up its own
+    // shared memory and then waits, as this grid does here, for the grids
+    // before it to complete before touching global memory.
+    ptx::launch_dependents();
     __syncthreads();
+    ptx::wait_prerequisite_grids();
 
     const uint32_t count = my_tile_count(a);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
+        const bool hint = (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
+        const uint64_t policy = hint ? ptx::policy_evict_first() : 0;
         for (uint32_t k = 0; k < count; ++k) {
             const uint32_t s = k % S, use = k / S;
             if (k >= S) {
@@ -278,6 +286,8 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
                 ptx::mbar_arrive_expect_tx(full, a.box_bytes);
                 if (MODE == kStore)
                     ptx::bulk_load(dst, a.packed + static_cast<size_t>(t) * a.box_bytes, a.box_bytes, full);
+                else if (hint)
+                    ptx::tma_load_hint<R>(dst, &src_map, c, full, policy);
                 else
                     ptx::tma_load<R>(dst, &src_map, c, full);
             }
@@ -288,6 +298,10 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
     }
 
     // ---------------------------------------------------------------- consumer
+    const bool store_hint = (a.l2_hints & (ATB_HINT_STORE_EVICT_FIRST | ATB_HINT_STORE_EVICT_LAST)) != 0;
+    const uint64_t store_policy = !store_hint ? 0
+                                  : (a.l2_hints & ATB_HINT_STORE_EVICT_FIRST) ? ptx::policy_evict_first()
+                                                                               : ptx::policy_evict_last();
     uint32_t next_release = 0;  // boxes [next_release, k) still have a group reading their stage
     uint32_t k = 0;
     bool failed = false;
@@ -335,6 +349,8 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
             ptx::fence_proxy_async_smem();
             if (MODE == kLoad)
                 ptx::bulk_store(a.packed + static_cast<size_t>(t) * a.box_bytes, src, a.box_bytes);
+            else if (store_hint)
+                ptx::tma_store_hint<R>(&dst_map, c, src, store_policy);
             else
                 ptx::tma_store<R>(&dst_map, c, src);
             ptx::bulk_commit();
@@ -402,6 +418,23 @@ size_t smem_bytes_for(const atb_tensor_map* m, uint32_t stages)
     return kStageAlignSwizzled + static_cast<size_t>(stages) * stage_bytes_for(m) + 16u * stages + sizeof(Control);
 }
 
+// Default pipeline shape, measured on GB300 round trips of a 512 MiB fp16
+// tensor (32 KiB and 16 KiB boxes): three stages per CTA, two store groups in
+// flight, and about 96 KiB of stages per SM (one CTA of 32 KiB boxes, two of
+// 16 KiB boxes).  A stage is then busy for one load and one store read, and
+// the ring always has a free stage for the next load.
+constexpr uint32_t kDefaultStages = 3;
+constexpr uint32_t kDefaultStoreGroups = 2;
+constexpr uint64_t kStageBytesPerSm = 96u * 1024u;
+constexpr uint64_t kMaxDefaultCtasPerSm = 8;
+
+uint32_t default_stages(const atb_tensor_map* m, const DeviceInfo& dev)
+{
+    uint32_t s = kDefaultStages;
+    while (s > 1 && smem_bytes_for(m, s) > static_cast<size_t>(dev.smem_optin)) --s;
+    return s;
+}
+
 std::mutex g_attr_mutex;
 
 atb_status prepare_kernel(KernelFn fn, const DeviceInfo& dev)
@@ -455,12 +488,12 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         return set_error(ATB_ERR_ARG, "%llu boxes in one call; the limit is 2^31 - 1",
                          static_cast<unsigned long long>(n_tiles));
 
-    const uint32_t stages = cfg && cfg->stages ? cfg->stages : 4;
-    if (stages < 1 || stages > kMaxStages)
-        return set_error(ATB_ERR_ARG, "stages = %u is outside 1..%u", stages, kMaxStages);
     DeviceInfo dev;
     atb_status st = current_device(&dev);
     if (st != ATB_OK) return st;
+    const uint32_t stages = cfg && cfg->stages ? cfg->stages : default_stages(shape, dev);
+    if (stages < 1 || stages > kMaxStages)
+        return set_error(ATB_ERR_ARG, "stages = %u is outside 1..%u", stages, kMaxStages);
     const size_t smem = smem_bytes_for(shape, stages);
     if (smem > static_cast<size_t>(dev.smem_optin))
         return set_error(ATB_ERR_SMEM_BUDGET,
@@ -483,7 +516,9 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         int fit = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, fn, kPipelineThreads, smem);
         if (e != cudaSuccess) return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-        per_sm = fit < 1 ? 1 : (fit > 2 ? 2 : static_cast<uint32_t>(fit));
+        uint64_t want = kStageBytesPerSm / (static_cast<uint64_t>(stages) * stage_bytes_for(shape));
+        want = want < 1 ? 1 : (want > kMaxDefaultCtasPerSm ? kMaxDefaultCtasPerSm : want);
+        per_sm = static_cast<uint32_t>(fit < 1 ? 1 : (static_cast<uint64_t>(fit) < want ? fit : want));
     }
     uint64_t grid = cfg && cfg->ctas ? cfg->ctas : static_cast<uint64_t>(dev.sm_count) * per_sm;
     if (grid > n_tiles) grid = n_tiles;
@@ -499,11 +534,12 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.box_bytes = shape->box_bytes;
     a.stage_bytes = stage_bytes_for(shape);
     a.stages = stages;
-    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : (stages < 8 ? stages : 8);
+    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : kDefaultStoreGroups;
     if (groups > stages) groups = stages;
     if (groups > 8) groups = 8;
     a.store_lag = groups - 1;
     a.contiguous = cfg && cfg->schedule == 1 ? 1u : 0u;
+    a.l2_hints = cfg ? cfg->l2_hints : 0u;
     a.swizzle_bits = swizzle_bits(shape->swizzle);
     for (uint32_t d = 0; d < rank; ++d) {
         a.box[d] = shape->box[d];
@@ -523,8 +559,17 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     memcpy(&src_map, (MODE == kStore ? dst : src)->map, sizeof src_map);
     memcpy(&dst_map, (MODE == kLoad ? src : dst)->map, sizeof dst_map);
 
-    fn<<<static_cast<unsigned>(grid), kPipelineThreads, smem, stream>>>(src_map, dst_map, a);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(kPipelineThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = cfg && cfg->no_pdl ? 0 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&lc, fn, src_map, dst_map, a);
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     return ATB_OK;
 }

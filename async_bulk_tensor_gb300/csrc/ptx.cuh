@@ -73,6 +73,35 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Lets the next grid on the stream be scheduled while this one finishes.
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until every grid this one depends on has completed and its memory
+// operations are visible; returns at once when there is no such grid.
+__device__ __forceinline__ void wait_prerequisite_grids()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---- L2 cache policies -----------------------------------------------------
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // ---- tensor-map copies -----------------------------------------------------
 __device__ __forceinline__ void prefetch_tensor_map(const void* map)
 {
@@ -175,6 +204,104 @@ __device__ __forceinline__ void tma_store<5>(const void* map, const int32_t* c, 
         "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
             reinterpret_cast<uint64_t>(map)),
         "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(src)
+        : "memory");
+}
+
+// Same copies with an L2 cache-eviction policy from createpolicy.
+template <int R>
+__device__ __forceinline__ void tma_load_hint(uint32_t dst, const void* map, const int32_t* c, uint32_t bar,
+                                              uint64_t policy);
+template <>
+__device__ __forceinline__ void tma_load_hint<1>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2}], [%3], %4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(bar), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load_hint<2>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(bar), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load_hint<3>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(bar), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load_hint<4>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(bar), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_load_hint<5>(uint32_t dst, const void* map, const int32_t* c, uint32_t bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+template <int R>
+__device__ __forceinline__ void tma_store_hint(const void* map, const int32_t* c, uint32_t src, uint64_t policy);
+template <>
+__device__ __forceinline__ void tma_store_hint<1>(const void* map, const int32_t* c, uint32_t src, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.1d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1}], [%2], %3;"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(src), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store_hint<2>(const void* map, const int32_t* c, uint32_t src, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(src), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store_hint<3>(const void* map, const int32_t* c, uint32_t src, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(src), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store_hint<4>(const void* map, const int32_t* c, uint32_t src, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3, %4}], [%5], %6;"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(src), "l"(policy)
+        : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_store_hint<5>(const void* map, const int32_t* c, uint32_t src, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3, %4, %5}], [%6], %7;"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(src), "l"(policy)
         : "memory");
 }
 

@@ -30,6 +30,11 @@
  *     default stream).  Host-detectable errors return before anything is
  *     launched; atb_last_error() then holds a sentence naming the rule, the
  *     dimension and the value.
+ *   - Pipeline kernels are launched with programmatic dependent launch: a
+ *     launch may be scheduled while the previous kernel on the stream drains,
+ *     sets up its shared memory, and waits for that kernel to complete (with
+ *     its memory visible) before it touches global memory.  Stream order is
+ *     therefore kept exactly; atb_launch.no_pdl = 1 turns the overlap off.
  *   - Errors raised inside a kernel (a wait that ran out of time, a misaligned
  *     box origin) are recorded in the device status block and reported by
  *     atb_device_status(); the kernel returns early instead of hanging.
@@ -118,15 +123,22 @@ typedef struct {
 
 /* Pipeline shape of one launch.  Zero fields take the library defaults. */
 typedef struct {
-    uint32_t stages;       /* shared-memory ring depth, 1..16 (default 4) */
+    uint32_t stages;       /* shared-memory ring depth, 1..16 (0 = 3, or fewer if 3 do not fit) */
     uint32_t ctas;         /* total CTAs; 0 = persistent grid of ctas_per_sm per SM */
-    uint32_t ctas_per_sm;  /* 0 = as many as shared memory allows, at most 2 */
+    uint32_t ctas_per_sm;  /* 0 = about 96 KiB of stages per SM (1..8), within what fits */
     uint32_t schedule;     /* 0 = box t goes to CTA t mod G; 1 = CTA b takes a contiguous run */
     uint32_t store_groups; /* bulk-store groups allowed in flight at once, 1..8, clamped to
-                              `stages` (0 = min(stages, 8)); a stage is recycled as soon as
+                              `stages` (0 = 2); a stage is recycled as soon as
                               the group that stores from it has finished reading it */
-    uint32_t reserved[3];
+    uint32_t l2_hints;     /* ATB_HINT_* bits: L2 eviction policy of the box loads and stores */
+    uint32_t no_pdl;       /* 1 = launch without programmatic dependent launch (see below) */
+    uint32_t reserved;
 } atb_launch;
+
+/* atb_launch.l2_hints bits */
+#define ATB_HINT_LOAD_EVICT_FIRST  1u
+#define ATB_HINT_STORE_EVICT_FIRST 2u
+#define ATB_HINT_STORE_EVICT_LAST  4u
 
 /* Contents of the device status block (one per device). */
 typedef struct {

@@ -1,0 +1,88 @@
+"""Host-side multi-process logic of the benchmark on CPU (gloo, world size 2).
+
+Every rank moves its own replica; the whole-job throughput is the bytes of
+all ranks divided by the slowest rank's time.  No GPU is involved here.
+"""
+import io
+import json
+import os
+import socket
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    d = bench.init_dist(world, "gloo")
+    seconds = [0.5, 2.0][rank]
+    units = [100.0, 300.0][rank]
+    bench.barrier(d)
+    total_units, max_seconds = bench.aggregate(d, seconds, units)
+    out.put((rank, total_units, max_seconds))
+    dist.destroy_process_group()
+
+
+def test_aggregate_takes_slowest_rank_and_sums_units():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    results = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, units, seconds in results:
+        assert units == 400.0 and seconds == 2.0
+
+
+def test_single_process_aggregate_is_identity():
+    import bench
+
+    assert bench.aggregate(None, 1.5, 42.0) == (42.0, 1.5)
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
+    import bench
+
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert buf.getvalue() == ""
+
+
+def test_reference_arm_prints_contract_line(monkeypatch):
+    import bench
+
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-tiles", "16"])
+    line = json.loads(buf.getvalue())
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_bench_rejects_short_warmup():
+    import bench
+
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
