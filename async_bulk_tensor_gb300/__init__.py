@@ -75,7 +75,7 @@ class Launch(ctypes.Structure):
         ("store_groups", ctypes.c_uint32),
         ("l2_hints", ctypes.c_uint32),
         ("no_pdl", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("poll_suspend_ns", ctypes.c_uint32),
     ]
 
 
@@ -119,6 +119,8 @@ def _load():
         "atb_set_wait_timeout_ns": (None, [U64]),
         "atb_selftest_wait_timeout": (S, [U64, P]),
         "atb_tile_roundtrip_noalloc": (S, [MapP, MapP, P, U64, LaunchP, P, ctypes.POINTER(DeviceReport)]),
+        "atb_tile_roundtrip_add_f32": (S, [MapP, MapP, P, U64, ctypes.c_float, LaunchP, P]),
+        "atb_tile_roundtrip_host": (S, [MapP, MapP, P, P, U32, LaunchP, P]),
         "atb_copy_cpasync": (S, [P, P, SZ, LaunchP, P]),
         "atb_copy_ldst_v4": (S, [P, P, SZ, LaunchP, P]),
         "atb_copy_memcpy": (S, [P, P, SZ, P]),
@@ -164,9 +166,10 @@ def _check(code: int, where: str):
 HINT_LOAD_EVICT_FIRST, HINT_STORE_EVICT_FIRST, HINT_STORE_EVICT_LAST = 1, 2, 4
 
 
-def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True) -> Launch:
+def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True,
+            poll_suspend_ns=0) -> Launch:
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
-                  store_groups, l2_hints, 0 if pdl else 1)
+                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns)
 
 
 def version() -> int:
@@ -227,6 +230,27 @@ def tile_roundtrip(src: TensorMap, dst: TensorMap, coords=None, n: int = 0, stre
     """``atb_tile_roundtrip``: store(dst, coords, load(src, coords)); ``coords=None`` = tile grid."""
     _check(lib.atb_tile_roundtrip(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
                                   ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_roundtrip")
+
+
+def tile_roundtrip_host(src: TensorMap, dst: TensorMap, h_src, h_dst, slabs: int = 0, stream=None, **launch):
+    """``atb_tile_roundtrip_host``: host source -> device -> boxes -> device -> host destination.
+
+    ``h_src``/``h_dst`` are host pointers (ints, or CPU tensors / numpy arrays
+    via ``data_ptr()``/``ctypes.data``), laid out as the device maps describe.
+    """
+    def hptr(x):
+        return x.ctypes.data if hasattr(x, "ctypes") and hasattr(x, "dtype") else _ptr(x)
+
+    _check(lib.atb_tile_roundtrip_host(ctypes.byref(src), ctypes.byref(dst), hptr(h_src), hptr(h_dst), int(slabs),
+                                       ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_roundtrip_host")
+
+
+def tile_roundtrip_add_f32(src: TensorMap, dst: TensorMap, addend: float, coords=None, n: int = 0, stream=None,
+                           **launch):
+    """``atb_tile_roundtrip_add_f32``: store(dst, coords, load(src, coords) + addend) in fp32."""
+    _check(lib.atb_tile_roundtrip_add_f32(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
+                                          float(addend), ctypes.byref(_launch(**launch)), _stream(stream)),
+           "atb_tile_roundtrip_add_f32")
 
 
 def tile_roundtrip_noalloc(src: TensorMap, dst: TensorMap, coords=None, n: int = 0, stream=None,

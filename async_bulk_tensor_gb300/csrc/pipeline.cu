@@ -40,7 +40,7 @@
 namespace atb {
 namespace {
 
-enum Mode : int { kRoundtrip = 0, kLoad = 1, kStore = 2 };
+enum Mode : int { kRoundtrip = 0, kLoad = 1, kStore = 2, kRoundtripAddF32 = 3 };
 
 struct PipeArgs {
     const int32_t* coords;  // n_tiles * rank origins, or null for the tile grid
@@ -52,7 +52,8 @@ struct PipeArgs {
     uint64_t dst_strides[ATB_MAX_RANK];
     uint32_t grid[ATB_MAX_RANK];  // boxes along each dimension (tile grid)
     uint32_t box[ATB_MAX_RANK];
-    uint32_t n_tiles;
+    uint32_t n_tiles;       // boxes in this launch
+    uint32_t tile_begin;    // index of its first box in the list or grid
     uint32_t esize;
     uint32_t box_bytes;
     uint32_t stage_bytes;
@@ -62,6 +63,7 @@ struct PipeArgs {
     uint32_t swizzle_bits;  // 0 none, 1 32B, 2 64B, 3 128B
     uint32_t dst_ragged_x;  // destination rows end inside a 16-byte chunk
     uint32_t l2_hints;      // ATB_HINT_* bits
+    uint32_t suspend_ns;    // mbarrier poll suspend-time hint, 0 = hardware default
 };
 
 // Shared-memory control words after the stage ring and the barriers.
@@ -86,12 +88,13 @@ __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int
 // Returns false on expiry or, when `abort` is non-null, once another role
 // has raised it.  The timer is read only after the first poll fails.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
-                                             const volatile uint32_t* abort)
+                                             const volatile uint32_t* abort, uint32_t suspend_ns = 0)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::global_timer_ns();
     for (;;) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (suspend_ns ? ptx::mbar_try_wait_suspend(bar, parity, suspend_ns) : ptx::mbar_try_wait(bar, parity))
+            return true;
         if (abort && *abort) return false;
         if (ptx::global_timer_ns() - t0 > timeout_ns) return false;
     }
@@ -120,10 +123,11 @@ __device__ __forceinline__ uint32_t my_tile_count(const PipeArgs& a)
     return b < a.n_tiles ? (a.n_tiles - b + G - 1) / G : 0;
 }
 
+// Index (in the list or grid) of this CTA's k-th box.
 __device__ __forceinline__ uint32_t tile_of(const PipeArgs& a, uint32_t k)
 {
-    if (a.contiguous) return blockIdx.x * ((a.n_tiles + gridDim.x - 1) / gridDim.x) + k;
-    return blockIdx.x + k * gridDim.x;
+    if (a.contiguous) return a.tile_begin + blockIdx.x * ((a.n_tiles + gridDim.x - 1) / gridDim.x) + k;
+    return a.tile_begin + blockIdx.x + k * gridDim.x;
 }
 
 // Origin of box t, innermost first: from the list, or from the row-major tile
@@ -182,38 +186,150 @@ __device__ __forceinline__ int store_kind(const PipeArgs& a, const int32_t (&c)[
     return plain ? kStorePlain : kStoreTensor;
 }
 
-// Whole-warp clipped store of one box image from shared memory.  The image
-// byte at offset o lives at o with its 16-byte chunk number (bits 4..6) XORed
-// by the low swizzle bits of its 128-byte line number (bits 7..9).
+// Clipped store of one box image from shared memory by `nthreads` threads,
+// 16 bytes at a time.  The swizzle moves whole 16-byte chunks (the chunk
+// number, bits 4..6 of the image offset, is XORed with the low swizzle bits of
+// the 128-byte line number, bits 7..9), and a box row starts on a 16-byte
+// boundary in both spaces (the origin's x is 16-byte aligned, strides are
+// multiples of 16), so a chunk that lies wholly inside the tensor moves as one
+// vector; only a chunk cut by the end of a row moves element by element.
 template <int R>
-__device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], const uint8_t* stage, uint32_t lane)
+__device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], const uint8_t* stage, uint32_t tid,
+                                uint32_t nthreads)
 {
-    const uint32_t elems = a.box_bytes / a.esize;
+    const uint32_t row_bytes = a.box[0] * a.esize;
+    const uint32_t chunks_per_row = row_bytes / 16;
+    const uint32_t rows = a.box_bytes / row_bytes;
+    const uint32_t q = 16 / a.esize;  // elements per chunk
     const uint32_t line_mask = (1u << a.swizzle_bits) - 1u;
-    for (uint32_t e = lane; e < elems; e += 32) {
-        uint32_t rest = e;
+    const int64_t dims0 = static_cast<int64_t>(a.dst_dims[0]);
+    for (uint32_t i = tid; i < rows * chunks_per_row; i += nthreads) {
+        const uint32_t row = i / chunks_per_row, j = i - row * chunks_per_row;
+        uint32_t rest = row;
         bool inside = true;
         uint64_t addr = 0;
 #pragma unroll
-        for (int d = 0; d < R; ++d) {
+        for (int d = 1; d < R; ++d) {
             const uint32_t k = rest % a.box[d];
             rest /= a.box[d];
             const int64_t g = static_cast<int64_t>(c[d]) + k;
             if (g < 0 || g >= static_cast<int64_t>(a.dst_dims[d])) inside = false;
             else addr += static_cast<uint64_t>(g) * a.dst_strides[d];
         }
-        if (!inside) continue;
-        const uint32_t o = e * a.esize;
-        const uint32_t so = o ^ (((o >> 7) & line_mask) << 4);
-        uint8_t* dst = a.dst_base + addr;
-        const uint8_t* src = stage + so;
-        switch (a.esize) {
-        case 1: *dst = *src; break;
-        case 2: *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(src); break;
-        case 4: *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src); break;
-        default: *reinterpret_cast<uint64_t*>(dst) = *reinterpret_cast<const uint64_t*>(src); break;
+        const int64_t x0 = static_cast<int64_t>(c[0]) + static_cast<int64_t>(j) * q;  // first element of the chunk
+        if (!inside || x0 < 0 || x0 >= dims0) continue;
+        const uint32_t o = row * row_bytes + 16 * j;
+        const uint8_t* src = stage + (o ^ (((o >> 7) & line_mask) << 4));
+        uint8_t* dst = a.dst_base + addr + static_cast<uint64_t>(x0) * a.esize;
+        if (x0 + q <= dims0) {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+            continue;
         }
+        for (uint32_t b = 0; b < static_cast<uint32_t>(dims0 - x0) * a.esize; ++b) dst[b] = src[b];
     }
+}
+
+// Shared-memory layout of one CTA: the stage ring (aligned to the swizzle
+// period), full[] and empty[] mbarriers, then the control words.
+struct Ring {
+    uint32_t base;      // shared address of stage 0
+    uint8_t* base_ptr;  // generic pointer to stage 0
+    uint32_t stages;
+    uint32_t stage_bytes;
+    uint32_t full0;     // full[s]  at full0 + 8 s
+    uint32_t empty0;    // empty[s] at empty0 + 8 s
+    Control* ctl;
+
+    __device__ uint32_t stage(uint32_t s) const { return base + s * stage_bytes; }
+    __device__ uint8_t* stage_ptr(uint32_t s) const { return base_ptr + s * stage_bytes; }
+    __device__ uint32_t full(uint32_t s) const { return full0 + 8 * s; }
+    __device__ uint32_t empty(uint32_t s) const { return empty0 + 8 * s; }
+    __device__ volatile uint32_t* abort_flag() const { return &ctl->abort; }
+};
+
+__device__ __forceinline__ Ring ring_layout(const PipeArgs& a, uint8_t* smem_raw)
+{
+    Ring r;
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    r.base = (raw + (kStageAlignSwizzled - 1)) & ~(kStageAlignSwizzled - 1);
+    r.base_ptr = smem_raw + (r.base - raw);
+    r.stages = a.stages;
+    r.stage_bytes = a.stage_bytes;
+    r.full0 = r.base + a.stages * a.stage_bytes;
+    r.empty0 = r.full0 + 8 * a.stages;
+    r.ctl = reinterpret_cast<Control*>(r.base_ptr + a.stages * a.stage_bytes + 16 * a.stages);
+    return r;
+}
+
+// Thread 0 initialises every barrier (one arrival each) and publishes the
+// initialisation to the async proxy; the caller follows with a block barrier.
+__device__ __forceinline__ void init_ring(const Ring& r)
+{
+    for (uint32_t s = 0; s < r.stages; ++s) {
+        ptx::mbar_init(r.full(s), 1);
+        ptx::mbar_init(r.empty(s), 1);
+    }
+    r.ctl->abort = 0;
+    r.ctl->issued = 0;
+    r.ctl->producer_done = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+}
+
+__device__ __forceinline__ void raise_abort(const PipeArgs& a, const Ring& r, uint32_t tile, int32_t where)
+{
+    if (!*r.abort_flag()) {
+        record_error(a.status, ATB_ERR_TIMEOUT, static_cast<int32_t>(tile), where);
+        *r.abort_flag() = 1;
+    }
+}
+
+// One producer thread: for its k-th box, wait until stage k mod N is free,
+// arm the stage's full barrier with the box's byte count and issue the copy.
+template <int MODE, int R>
+__device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, const Ring& r, uint32_t count)
+{
+    const bool hint = (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
+    const uint64_t policy = hint ? ptx::policy_evict_first() : 0;
+    const uint32_t S = r.stages;
+    for (uint32_t k = 0; k < count; ++k) {
+        const uint32_t s = k % S, use = k / S;
+        if (k >= S && !wait_bounded(r.empty(s), (use - 1) & 1, a.timeout_ns, r.abort_flag(), a.suspend_ns)) {
+            raise_abort(a, r, tile_of(a, k), kWhereProducerWait);
+            break;
+        }
+        const uint32_t t = tile_of(a, k);
+        int32_t c[R];
+        tile_origin<R>(a, t, c);
+        const int32_t bad = origin_error<R>(a, c);
+        if (bad) {
+            record_error(a.status, bad, static_cast<int32_t>(t), kWhereProducerIssue);
+            ptx::mbar_arrive(r.full(s));  // completes the phase with no bytes; consumers skip the box
+        } else {
+            ptx::mbar_arrive_expect_tx(r.full(s), a.box_bytes);
+            if (MODE == kStore)
+                ptx::bulk_load(r.stage(s), a.packed + static_cast<size_t>(t) * a.box_bytes, a.box_bytes, r.full(s));
+            else if (hint)
+                ptx::tma_load_hint<R>(r.stage(s), &src_map, c, r.full(s), policy);
+            else
+                ptx::tma_load<R>(r.stage(s), &src_map, c, r.full(s));
+        }
+        *reinterpret_cast<volatile uint32_t*>(&r.ctl->issued) = k + 1;
+    }
+    *reinterpret_cast<volatile uint32_t*>(&r.ctl->producer_done) = 1;
+}
+
+// After a failed wait at box k: stop the producer, then wait (bounded) for
+// every load it already started so that no copy lands in shared memory after
+// the CTA exits.  Called by one thread, after bulk_wait_all().
+__device__ void drain_after_failure(const PipeArgs& a, const Ring& r, uint32_t k)
+{
+    raise_abort(a, r, tile_of(a, k), kWhereConsumerWait);
+    const uint64_t deadline = ptx::global_timer_ns() + a.timeout_ns;
+    while (!*reinterpret_cast<volatile uint32_t*>(&r.ctl->producer_done) && ptx::global_timer_ns() < deadline) {
+    }
+    const uint32_t issued = *reinterpret_cast<volatile uint32_t*>(&r.ctl->issued);
+    for (uint32_t j = k; j < issued; ++j) wait_until(r.full(j % r.stages), (j / r.stages) & 1, deadline);
 }
 
 template <int MODE, int R>
@@ -222,27 +338,10 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
                          const PipeArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = ptx::smem_addr(smem_raw);
-    const uint32_t ring = (raw + (kStageAlignSwizzled - 1)) & ~(kStageAlignSwizzled - 1);
-    uint8_t* const ring_ptr = smem_raw + (ring - raw);
-    const uint32_t S = a.stages;
-    const uint32_t full0 = ring + S * a.stage_bytes;  // full[s]  at full0 + 8 s
-    const uint32_t empty0 = full0 + 8 * S;            // empty[s] at empty0 + 8 s
-    Control* ctl = reinterpret_cast<Control*>(ring_ptr + S * a.stage_bytes + 16 * S);
-    volatile uint32_t* abort_flag = &ctl->abort;
-
+    const Ring r = ring_layout(a, smem_raw);
+    const uint32_t S = r.stages;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < S; ++s) {
-            ptx::mbar_init(full0 + 8 * s, 1);
-            ptx::mbar_init(empty0 + 8 * s, 1);
-        }
-        ctl->abort = 0;
-        ctl->issued = 0;
-        ctl->producer_done = 0;
-        ptx::fence_barrier_init();
-        ptx::fence_proxy_async_smem();
-    }
+    if (threadIdx.x == 0) init_ring(r);
     if (threadIdx.x == 32) {
         if (MODE != kStore) ptx::prefetch_tensor_map(&src_map);
         if (MODE != kLoad) ptx::prefetch_tensor_map(&dst_map);
@@ -257,43 +356,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
     const uint32_t count = my_tile_count(a);
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane != 0) return;
-        const bool hint = (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
-        const uint64_t policy = hint ? ptx::policy_evict_first() : 0;
-        for (uint32_t k = 0; k < count; ++k) {
-            const uint32_t s = k % S, use = k / S;
-            if (k >= S) {
-                if (!wait_bounded(empty0 + 8 * s, (use - 1) & 1, a.timeout_ns, abort_flag)) {
-                    if (!*abort_flag) {
-                        record_error(a.status, ATB_ERR_TIMEOUT, static_cast<int32_t>(tile_of(a, k)),
-                                     kWhereProducerWait);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-            }
-            const uint32_t t = tile_of(a, k);
-            const uint32_t full = full0 + 8 * s;
-            const uint32_t dst = ring + s * a.stage_bytes;
-            int32_t c[R];
-            tile_origin<R>(a, t, c);
-            const int32_t bad = origin_error<R>(a, c);
-            if (bad) {
-                record_error(a.status, bad, static_cast<int32_t>(t), kWhereProducerIssue);
-                ptx::mbar_arrive(full);  // completes the phase with no bytes; the consumer skips the box
-            } else {
-                ptx::mbar_arrive_expect_tx(full, a.box_bytes);
-                if (MODE == kStore)
-                    ptx::bulk_load(dst, a.packed + static_cast<size_t>(t) * a.box_bytes, a.box_bytes, full);
-                else if (hint)
-                    ptx::tma_load_hint<R>(dst, &src_map, c, full, policy);
-                else
-                    ptx::tma_load<R>(dst, &src_map, c, full);
-            }
-            *reinterpret_cast<volatile uint32_t*>(&ctl->issued) = k + 1;
-        }
-        *reinterpret_cast<volatile uint32_t*>(&ctl->producer_done) = 1;
+        if (lane == 0) producer_loop<MODE, R>(a, src_map, r, count);
         return;
     }
 
@@ -307,8 +370,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
     bool failed = false;
     for (; k < count; ++k) {
         const uint32_t s = k % S, parity = (k / S) & 1;
-        const uint32_t full = full0 + 8 * s;
-        const bool ok = wait_bounded(full, parity, a.timeout_ns, abort_flag);
+        const bool ok = wait_bounded(r.full(s), parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
         if (!__all_sync(0xffffffffu, ok)) {
             failed = true;
             break;
@@ -317,64 +379,116 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
         int32_t c[R];
         tile_origin<R>(a, t, c);
         const bool skip = origin_error<R>(a, c) != 0;
-        const int kind = MODE == kLoad ? kStoreTensor : (skip ? kStoreNothing : store_kind<R>(a, c));
-        const uint32_t src = ring + s * a.stage_bytes;
+        // kLoad: kStoreTensor means "drain the image to the packed buffer"
+        const int kind = skip ? kStoreNothing : (MODE == kLoad ? kStoreTensor : store_kind<R>(a, c));
 
-        if (MODE != kLoad && kind != kStoreTensor) {
-            // Rare path: retire every pending group so that stage bookkeeping
-            // stays in order, then write (or drop) this box without the engine.
-            if (lane == 0) {
-                ptx::bulk_wait_read<0>();
-                for (; next_release < k; ++next_release) ptx::mbar_arrive(empty0 + 8 * (next_release % S));
-            }
+        if (kind == kStorePlain) {
+            // boxes the engine may not store: the warp writes them itself
+            plain_store_box<R>(a, c, r.stage_ptr(s), lane, 32);
             __syncwarp();
-            if (kind == kStorePlain) plain_store_box<R>(a, c, ring_ptr + s * a.stage_bytes, lane);
-            __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(empty0 + 8 * s);
-                next_release = k + 1;
-            }
-            continue;
-        }
-        if (MODE == kLoad && skip) {
-            if (lane == 0) {
-                ptx::bulk_wait_read<0>();
-                for (; next_release < k; ++next_release) ptx::mbar_arrive(empty0 + 8 * (next_release % S));
-                ptx::mbar_arrive(empty0 + 8 * s);
-                next_release = k + 1;
-            }
-            continue;
         }
         if (lane == 0) {
-            ptx::fence_proxy_async_smem();
-            if (MODE == kLoad)
-                ptx::bulk_store(a.packed + static_cast<size_t>(t) * a.box_bytes, src, a.box_bytes);
-            else if (store_hint)
-                ptx::tma_store_hint<R>(&dst_map, c, src, store_policy);
-            else
-                ptx::tma_store<R>(&dst_map, c, src);
+            if (kind == kStoreTensor) {
+                ptx::fence_proxy_async_smem();
+                if (MODE == kLoad)
+                    ptx::bulk_store(a.packed + static_cast<size_t>(t) * a.box_bytes, r.stage(s), a.box_bytes);
+                else if (store_hint)
+                    ptx::tma_store_hint<R>(&dst_map, c, r.stage(s), store_policy);
+                else
+                    ptx::tma_store<R>(&dst_map, c, r.stage(s));
+            }
+            // One group per box (an empty one when the engine stores nothing),
+            // so that the groups still reading map to boxes [k - lag, k].
             ptx::bulk_commit();
             ptx::bulk_wait_read_le(a.store_lag);
-            for (; next_release + a.store_lag <= k; ++next_release)
-                ptx::mbar_arrive(empty0 + 8 * (next_release % S));
+            for (; next_release + a.store_lag <= k; ++next_release) ptx::mbar_arrive(r.empty(next_release % S));
         }
     }
 
     if (lane != 0) return;
     ptx::bulk_wait_all();
-    if (!failed) return;
+    if (failed) drain_after_failure(a, r, k);
+}
 
-    // Failure: stop the producer, then wait (bounded) for every load it
-    // already started so that no copy lands in shared memory after exit.
-    if (!*abort_flag) {
-        record_error(a.status, ATB_ERR_TIMEOUT, static_cast<int32_t>(tile_of(a, k)), kWhereConsumerWait);
-        *abort_flag = 1;
+// Round trip with an elementwise fp32 update in shared memory between the load
+// and the store ("Day 76: The Tensor Memory Accelerator (TMA)", "Exercise" and
+// "Solution": the threads change the tile in shared memory, every writer
+// publishes its writes across the proxy line with fence.proxy.async, the group
+// meets at a barrier, and one thread issues the tensor store).  Warp 0 lane 0
+// produces; warps 1..kTransformWarps update the stage, lane 0 of warp 1
+// issues the store.  Each element becomes x + addend in round-to-nearest fp32.
+template <int R>
+__global__ void __launch_bounds__(kTransformThreads, 1)
+    tile_add_f32_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
+                        const PipeArgs a, float addend)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Ring r = ring_layout(a, smem_raw);
+    const uint32_t S = r.stages;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) init_ring(r);
+    if (threadIdx.x == 32) {
+        ptx::prefetch_tensor_map(&src_map);
+        ptx::prefetch_tensor_map(&dst_map);
     }
-    const uint64_t deadline = ptx::global_timer_ns() + a.timeout_ns;
-    while (!*reinterpret_cast<volatile uint32_t*>(&ctl->producer_done) && ptx::global_timer_ns() < deadline) {
+    ptx::launch_dependents();
+    __syncthreads();
+    ptx::wait_prerequisite_grids();
+
+    const uint32_t count = my_tile_count(a);
+    if (warp == 0) {
+        if (lane == 0) producer_loop<kRoundtrip, R>(a, src_map, r, count);
+        return;
     }
-    const uint32_t issued = *reinterpret_cast<volatile uint32_t*>(&ctl->issued);
-    for (uint32_t j = k; j < issued; ++j) wait_until(full0 + 8 * (j % S), (j / S) & 1, deadline);
+
+    const uint32_t ct = threadIdx.x - 32;  // consumer thread 0 .. kConsumerThreads-1
+    const uint32_t chunks = a.box_bytes / 16;
+    uint32_t next_release = 0;
+    uint32_t k = 0;
+    bool failed = false;
+    for (; k < count; ++k) {
+        const uint32_t s = k % S, parity = (k / S) & 1;
+        const bool ok = wait_bounded(r.full(s), parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
+        if (!__all_sync(0xffffffffu, ok)) {
+            failed = true;
+        }
+        // every consumer warp must agree before any of them leaves the loop
+        if (ptx::named_barrier_or(1, kConsumerThreads, failed)) {
+            failed = true;
+            break;
+        }
+        const uint32_t t = tile_of(a, k);
+        int32_t c[R];
+        tile_origin<R>(a, t, c);
+        const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
+        if (kind != kStoreNothing) {
+            // generic-proxy update of the landed box; element order is irrelevant
+            const uint32_t base = r.stage(s);
+            for (uint32_t j = ct; j < chunks; j += kConsumerThreads) {
+                float v[4];
+                ptx::ld_shared_v4_f32(base + 16 * j, v);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = __fadd_rn(v[e], addend);
+                ptx::st_shared_v4_f32(base + 16 * j, v);
+            }
+            ptx::fence_proxy_async_smem();  // each writer publishes its own writes to the async proxy
+        }
+        ptx::named_barrier_sync(1, kConsumerThreads);
+        if (kind == kStorePlain) {
+            plain_store_box<R>(a, c, r.stage_ptr(s), ct, kConsumerThreads);
+            ptx::named_barrier_sync(1, kConsumerThreads);  // every reader is done with the stage
+        }
+        if (ct == 0) {
+            if (kind == kStoreTensor) ptx::tma_store<R>(&dst_map, c, r.stage(s));
+            ptx::bulk_commit();  // one group per box, empty when the engine stores nothing
+            ptx::bulk_wait_read_le(a.store_lag);
+            for (; next_release + a.store_lag <= k; ++next_release) ptx::mbar_arrive(r.empty(next_release % S));
+        }
+    }
+
+    if (ct != 0) return;
+    ptx::bulk_wait_all();
+    if (failed) drain_after_failure(a, r, k);
 }
 
 // Self-test of the bounded wait: nothing ever completes this barrier.
@@ -392,6 +506,7 @@ __global__ void wait_timeout_selftest_kernel(DeviceStatus* st, uint64_t timeout_
 }
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PipeArgs);
+using AddKernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PipeArgs, float);
 
 template <int MODE>
 KernelFn kernel_for_rank(uint32_t rank)
@@ -402,6 +517,17 @@ KernelFn kernel_for_rank(uint32_t rank)
     case 3: return tile_pipeline_kernel<MODE, 3>;
     case 4: return tile_pipeline_kernel<MODE, 4>;
     default: return tile_pipeline_kernel<MODE, 5>;
+    }
+}
+
+AddKernelFn add_kernel_for_rank(uint32_t rank)
+{
+    switch (rank) {
+    case 1: return tile_add_f32_kernel<1>;
+    case 2: return tile_add_f32_kernel<2>;
+    case 3: return tile_add_f32_kernel<3>;
+    case 4: return tile_add_f32_kernel<4>;
+    default: return tile_add_f32_kernel<5>;
     }
 }
 
@@ -437,40 +563,45 @@ uint32_t default_stages(const atb_tensor_map* m, const DeviceInfo& dev)
 
 std::mutex g_attr_mutex;
 
-atb_status prepare_kernel(KernelFn fn, const DeviceInfo& dev)
+atb_status prepare_kernel(const void* fn, const DeviceInfo& dev)
 {
     // Opt every instantiation into the full per-block shared memory once per device.
     static const void* done[64][64];
     static int n_done[64];
     std::lock_guard<std::mutex> lock(g_attr_mutex);
     for (int i = 0; i < n_done[dev.device]; ++i)
-        if (done[dev.device][i] == reinterpret_cast<const void*>(fn)) return ATB_OK;
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
+        if (done[dev.device][i] == fn) return ATB_OK;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
     if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
-    if (n_done[dev.device] < 64) done[dev.device][n_done[dev.device]++] = reinterpret_cast<const void*>(fn);
+    if (n_done[dev.device] < 64) done[dev.device][n_done[dev.device]++] = fn;
     return ATB_OK;
 }
 
 // `caller_status`, when given, receives the kernel's error record instead of
 // the device's lazily allocated status block.
+// Launches one pipeline over boxes [first, first + count) of the list or grid
+// (count = UINT64_MAX: all of them).
 template <int MODE>
 atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst, const int32_t* coords, uint64_t n,
                            void* packed, const atb_launch* cfg, cudaStream_t stream,
-                           DeviceStatus* caller_status = nullptr)
+                           DeviceStatus* caller_status = nullptr, float addend = 0.0f, uint64_t first = 0,
+                           uint64_t count = UINT64_MAX)
 {
     clear_error();
     const atb_tensor_map* shape = MODE == kStore ? dst : src;
     if ((MODE != kStore && !map_is_valid(src)) || (MODE != kLoad && !map_is_valid(dst)))
         return set_error(ATB_ERR_ARG, "tensor map is NULL or was not produced by atb_encode_tiled");
-    if (MODE == kRoundtrip) {
+    if (MODE == kRoundtripAddF32 && (src->dtype != ATB_F32 || dst->dtype != ATB_F32))
+        return set_error(ATB_ERR_DTYPE, "the fp32 update needs ATB_F32 maps (got types %u and %u)", src->dtype,
+                         dst->dtype);
+    if (MODE == kRoundtrip || MODE == kRoundtripAddF32) {
         bool same = src->rank == dst->rank && src->esize == dst->esize && src->swizzle == dst->swizzle;
         for (uint32_t d = 0; same && d < src->rank; ++d) same = src->box[d] == dst->box[d];
         if (!same)
             return set_error(ATB_ERR_ARG,
                              "source and destination maps differ in rank, element size, box or swizzle");
     }
-    if (MODE != kRoundtrip) {
+    if (MODE == kLoad || MODE == kStore) {
         if (!packed) return set_error(ATB_ERR_ARG, "packed buffer is NULL");
         if (reinterpret_cast<uintptr_t>(packed) % 16)
             return set_error(ATB_ERR_SMEM_ALIGN, "packed buffer %p is not 16-byte aligned", packed);
@@ -487,6 +618,9 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     if (n_tiles >= 0x80000000ull)
         return set_error(ATB_ERR_ARG, "%llu boxes in one call; the limit is 2^31 - 1",
                          static_cast<unsigned long long>(n_tiles));
+    if (first > n_tiles) return set_error(ATB_ERR_ARG, "box range starts past the last box");
+    const uint64_t all_tiles = n_tiles;
+    n_tiles = count < all_tiles - first ? count : all_tiles - first;
 
     DeviceInfo dev;
     atb_status st = current_device(&dev);
@@ -507,14 +641,16 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         if (st != ATB_OK) return st;
     }
 
-    KernelFn fn = kernel_for_rank<MODE>(rank);
+    const void* fn = MODE == kRoundtripAddF32 ? reinterpret_cast<const void*>(add_kernel_for_rank(rank))
+                                              : reinterpret_cast<const void*>(kernel_for_rank<MODE == kRoundtripAddF32 ? kRoundtrip : MODE>(rank));
+    const uint32_t threads = MODE == kRoundtripAddF32 ? kTransformThreads : kPipelineThreads;
     st = prepare_kernel(fn, dev);
     if (st != ATB_OK) return st;
 
     uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm : 0;
     if (!per_sm) {
         int fit = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, fn, kPipelineThreads, smem);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, fn, threads, smem);
         if (e != cudaSuccess) return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         uint64_t want = kStageBytesPerSm / (static_cast<uint64_t>(stages) * stage_bytes_for(shape));
         want = want < 1 ? 1 : (want > kMaxDefaultCtasPerSm ? kMaxDefaultCtasPerSm : want);
@@ -530,6 +666,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.status = status;
     a.timeout_ns = wait_timeout_ns();
     a.n_tiles = static_cast<uint32_t>(n_tiles);
+    a.tile_begin = static_cast<uint32_t>(first);
     a.esize = shape->esize;
     a.box_bytes = shape->box_bytes;
     a.stage_bytes = stage_bytes_for(shape);
@@ -540,12 +677,13 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.store_lag = groups - 1;
     a.contiguous = cfg && cfg->schedule == 1 ? 1u : 0u;
     a.l2_hints = cfg ? cfg->l2_hints : 0u;
+    a.suspend_ns = cfg ? cfg->poll_suspend_ns : 0u;
     a.swizzle_bits = swizzle_bits(shape->swizzle);
     for (uint32_t d = 0; d < rank; ++d) {
         a.box[d] = shape->box[d];
         a.grid[d] = static_cast<uint32_t>((shape->dims[d] + shape->box[d] - 1) / shape->box[d]);
     }
-    if (MODE != kLoad) {
+    if (MODE != kLoad) {  // every mode that writes a tensor
         a.dst_base = reinterpret_cast<uint8_t*>(dst->base);
         for (uint32_t d = 0; d < rank; ++d) {
             a.dst_dims[d] = dst->dims[d];
@@ -561,7 +699,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
 
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(static_cast<unsigned>(grid));
-    lc.blockDim = dim3(kPipelineThreads);
+    lc.blockDim = dim3(threads);
     lc.dynamicSmemBytes = smem;
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -569,7 +707,12 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = cfg && cfg->no_pdl ? 0 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&lc, fn, src_map, dst_map, a);
+    cudaError_t e;
+    if (MODE == kRoundtripAddF32)
+        e = cudaLaunchKernelEx(&lc, add_kernel_for_rank(rank), src_map, dst_map, a, addend);
+    else
+        e = cudaLaunchKernelEx(&lc, kernel_for_rank<MODE == kRoundtripAddF32 ? kRoundtrip : MODE>(rank), src_map,
+                               dst_map, a);
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     return ATB_OK;
 }
@@ -603,12 +746,150 @@ atb_status noalloc_scratch_address(const DeviceInfo& dev, void** out)
     return ATB_OK;
 }
 
+// ---- host-resident round trip ------------------------------------------------
+// Per-device streams and events that overlap the host-to-device copies, the
+// round trips and the device-to-host copies of atb_tile_roundtrip_host.
+constexpr uint32_t kMaxHostSlabs = 64;
+constexpr uint32_t kDefaultHostSlabs = 8;
+
+struct HostPipe {
+    bool ready;
+    cudaStream_t in, out;
+    cudaEvent_t start, end;
+    cudaEvent_t landed[kMaxHostSlabs], moved[kMaxHostSlabs];
+};
+
+std::mutex g_host_mutex;
+HostPipe g_host_pipe[64];
+
+atb_status host_pipe(int device, HostPipe** out)
+{
+    if (device < 0 || device >= 64) return set_error(ATB_ERR_ARG, "device ordinal %d out of range", device);
+    HostPipe& p = g_host_pipe[device];
+    if (!p.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.end, cudaEventDisableTiming);
+        for (uint32_t j = 0; e == cudaSuccess && j < kMaxHostSlabs; ++j) {
+            e = cudaEventCreateWithFlags(&p.landed[j], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.moved[j], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return cuda_error(e, "creating the host-transfer streams and events");
+        p.ready = true;
+    }
+    *out = &p;
+    return ATB_OK;
+}
+
+// Bytes of dimensions 0..d-1 of a map, from element 0 to one past the last.
+uint64_t inner_span(const atb_tensor_map* m, uint32_t d)
+{
+    uint64_t span = m->esize;
+    for (uint32_t i = 1; i < d; ++i) span += (m->dims[i] - 1) * m->strides[i];
+    return span + (d > 0 ? (m->dims[0] - 1) * m->esize : 0);
+}
+
+// Byte range [lo, hi) that holds rows [r0, r1) of the outermost dimension.
+void slab_bytes(const atb_tensor_map* m, uint64_t r0, uint64_t r1, uint64_t* lo, uint64_t* hi)
+{
+    const uint32_t L = m->rank - 1;
+    const uint64_t stride = L ? m->strides[L] : m->esize;
+    const uint64_t inner = L ? inner_span(m, L) : m->esize;
+    *lo = r0 * stride;
+    *hi = (r1 - 1) * stride + inner;
+}
+
 }  // namespace
 }  // namespace atb
 
 using namespace atb;
 
 extern "C" {
+
+atb_status atb_tile_roundtrip_host(const atb_tensor_map* src, const atb_tensor_map* dst, const void* h_src,
+                                   void* h_dst, uint32_t slabs, const atb_launch* launch, atb_stream_t stream)
+{
+    clear_error();
+    if (!map_is_valid(src) || !map_is_valid(dst))
+        return set_error(ATB_ERR_ARG, "tensor map is NULL or was not produced by atb_encode_tiled");
+    if (!h_src || !h_dst) return set_error(ATB_ERR_ARG, "host source or destination is NULL");
+    if (src->rank != dst->rank) return set_error(ATB_ERR_ARG, "source and destination ranks differ");
+    for (uint32_t d = 0; d < src->rank; ++d)
+        if (src->dims[d] != dst->dims[d])
+            return set_error(ATB_ERR_ARG, "source and destination extents differ along dimension %u", d);
+    DeviceInfo dev;
+    atb_status st = current_device(&dev);
+    if (st != ATB_OK) return st;
+
+    const uint32_t L = src->rank - 1;
+    const uint64_t tiles_l = (src->dims[L] + src->box[L] - 1) / src->box[L];
+    const uint64_t per_row = atb_grid_tiles(src) / tiles_l;
+    // Slabs are contiguous byte ranges only when the outermost dimension
+    // steps over everything inside it.
+    const bool nested = L == 0 || (src->strides[L] >= inner_span(src, L) && dst->strides[L] >= inner_span(dst, L));
+    uint64_t n = slabs ? slabs : kDefaultHostSlabs;
+    if (n > kMaxHostSlabs) n = kMaxHostSlabs;
+    if (n > tiles_l) n = tiles_l;
+    if (!nested) n = 1;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    HostPipe* p = nullptr;
+    st = host_pipe(dev.device, &p);
+    if (st != ATB_OK) return st;
+    cudaError_t e = cudaEventRecord(p->start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->in, p->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->start, 0);
+    if (e != cudaSuccess) return cuda_error(e, "ordering the transfer streams after the caller's stream");
+
+    const uint8_t* hs = static_cast<const uint8_t*>(h_src);
+    uint8_t* hd = static_cast<uint8_t*>(h_dst);
+    uint8_t* ds = reinterpret_cast<uint8_t*>(src->base);
+    uint8_t* dd = reinterpret_cast<uint8_t*>(dst->base);
+    for (uint64_t j = 0; j < n; ++j) {  // host -> device, slab by slab
+        const uint64_t t0 = tiles_l * j / n, t1 = tiles_l * (j + 1) / n;
+        uint64_t lo, hi;
+        if (n == 1) {
+            lo = 0;
+            hi = inner_span(src, src->rank);
+        } else {
+            const uint64_t r1 = t1 * src->box[L] < src->dims[L] ? t1 * src->box[L] : src->dims[L];
+            slab_bytes(src, t0 * src->box[L], r1, &lo, &hi);
+        }
+        e = cudaMemcpyAsync(ds + lo, hs + lo, hi - lo, cudaMemcpyHostToDevice, p->in);
+        if (e == cudaSuccess) e = cudaEventRecord(p->landed[j], p->in);
+        if (e != cudaSuccess) return cuda_error(e, "host-to-device slab copy");
+    }
+    for (uint64_t j = 0; j < n; ++j) {  // round trip of each slab's boxes once its rows have landed
+        const uint64_t t0 = tiles_l * j / n, t1 = tiles_l * (j + 1) / n;
+        e = cudaStreamWaitEvent(s, p->landed[j], 0);
+        if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent");
+        st = launch_pipeline<kRoundtrip>(src, dst, nullptr, 0, nullptr, launch, s, nullptr, 0.0f, t0 * per_row,
+                                         (t1 - t0) * per_row);
+        if (st != ATB_OK) return st;
+        e = cudaEventRecord(p->moved[j], s);
+        if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord");
+    }
+    for (uint64_t j = 0; j < n; ++j) {  // device -> host of each slab once its boxes are stored
+        const uint64_t t0 = tiles_l * j / n, t1 = tiles_l * (j + 1) / n;
+        uint64_t lo, hi;
+        if (n == 1) {
+            lo = 0;
+            hi = inner_span(dst, dst->rank);
+        } else {
+            const uint64_t r1 = t1 * dst->box[L] < dst->dims[L] ? t1 * dst->box[L] : dst->dims[L];
+            slab_bytes(dst, t0 * dst->box[L], r1, &lo, &hi);
+        }
+        e = cudaStreamWaitEvent(p->out, p->moved[j], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(hd + lo, dd + lo, hi - lo, cudaMemcpyDeviceToHost, p->out);
+        if (e != cudaSuccess) return cuda_error(e, "device-to-host slab copy");
+    }
+    e = cudaEventRecord(p->end, p->out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, p->end, 0);
+    if (e != cudaSuccess) return cuda_error(e, "ordering the caller's stream after the transfers");
+    return ATB_OK;
+}
 
 atb_status atb_tile_roundtrip_noalloc(const atb_tensor_map* src, const atb_tensor_map* dst, const int32_t* d_coords,
                                       uint64_t n, const atb_launch* launch, atb_stream_t stream,
@@ -673,6 +954,13 @@ atb_status atb_tile_roundtrip(const atb_tensor_map* src, const atb_tensor_map* d
 {
     return launch_pipeline<kRoundtrip>(src, dst, d_coords, n, nullptr, launch,
                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+atb_status atb_tile_roundtrip_add_f32(const atb_tensor_map* src, const atb_tensor_map* dst, const int32_t* d_coords,
+                                      uint64_t n, float addend, const atb_launch* launch, atb_stream_t stream)
+{
+    return launch_pipeline<kRoundtripAddF32>(src, dst, d_coords, n, nullptr, launch,
+                                             reinterpret_cast<cudaStream_t>(stream), nullptr, addend);
 }
 
 atb_status atb_selftest_wait_timeout(uint64_t timeout_ns, atb_stream_t stream)

@@ -143,6 +143,15 @@ def normal_f16_bytes(n_elems: int, seed: int) -> np.ndarray:
     return x.view(torch.uint8).numpy()
 
 
+def finite_f32_bytes(n_elems: int, seed: int) -> np.ndarray:
+    """Random fp32 bit patterns with every Inf/NaN pattern made finite
+    (exponent 0xFF -> 0x7F); zeros of both signs and denormals are kept."""
+    bits = random_bytes(4 * n_elems, seed).view(np.uint32).copy()
+    inf_nan = (bits & np.uint32(0x7F800000)) == np.uint32(0x7F800000)
+    bits[inf_nan] &= np.uint32(0xBFFFFFFF)
+    return bits.view(np.uint8)
+
+
 def storage(w: Workload, seed: int | None = None) -> np.ndarray:
     """The workload's backing bytes (uint8, ``w.storage_bytes`` long)."""
     s = w.seed if seed is None else seed

@@ -132,7 +132,7 @@ typedef struct {
                               the group that stores from it has finished reading it */
     uint32_t l2_hints;     /* ATB_HINT_* bits: L2 eviction policy of the box loads and stores */
     uint32_t no_pdl;       /* 1 = launch without programmatic dependent launch (see below) */
-    uint32_t reserved;
+    uint32_t poll_suspend_ns; /* mbarrier waits: suspend-time hint per poll in ns (0 = hardware default) */
 } atb_launch;
 
 /* atb_launch.l2_hints bits */
@@ -282,6 +282,58 @@ atb_status atb_tile_store(const atb_tensor_map* dst, const int32_t* d_coords, ui
 atb_status atb_tile_roundtrip(const atb_tensor_map* src, const atb_tensor_map* dst,
                               const int32_t* d_coords, uint64_t n, const atb_launch* launch,
                               atb_stream_t stream);
+
+/*
+ * atb_tile_roundtrip_host -- the full-grid round trip for tensors that live
+ * in host memory: copy the source host -> device, move every box through
+ * shared memory into the destination, copy the destination device -> host.
+ *
+ * The tile grid is cut into `slabs` runs of whole box rows along the
+ * outermost dimension.  Slab j's host-to-device copy, its boxes' round trip
+ * and its device-to-host copy run on three streams ordered by events, so the
+ * copies of one slab overlap the work of the others ([L04] "Why this only
+ * pays off inside a pipeline", applied to whole slabs).  The call is ordered
+ * after earlier work on `stream`, and later work on `stream` runs after it.
+ *
+ *   src, dst  maps over caller-owned DEVICE buffers (staging); equal rank and
+ *             extents; box, element size and swizzle as for
+ *             atb_tile_roundtrip
+ *   h_src     host memory laid out exactly as `src` describes its device
+ *             buffer (same byte offsets); pinned memory lets copies overlap
+ *   h_dst     host memory laid out as `dst` describes its device buffer;
+ *             bytes between rows (padding) may be overwritten with the
+ *             device buffer's contents
+ *   slabs     0 = 8; clamped to 1..64 and to the number of box rows.  When
+ *             the outermost stride does not step over the whole inner span
+ *             (a permuted view), the call uses one slab.
+ * Not for concurrent use from several host threads on one device (the
+ * per-device streams and events are shared; calls serialise their enqueue).
+ */
+atb_status atb_tile_roundtrip_host(const atb_tensor_map* src, const atb_tensor_map* dst,
+                                   const void* h_src, void* h_dst, uint32_t slabs,
+                                   const atb_launch* launch, atb_stream_t stream);
+
+/*
+ * atb_tile_roundtrip_add_f32 -- the round trip with an elementwise fp32 update
+ * in shared memory: every element of each landed box becomes x + addend
+ * (IEEE round-to-nearest, denormals kept) before the box is stored.
+ *
+ * [D76] "Exercise", "Hint 1", "Hint 2" and "Solution": the threads change
+ * the tile in shared memory through the generic proxy, each writer then
+ * publishes its writes with fence.proxy.async, the group meets at a barrier
+ * and one thread issues the tensor store, completed through a bulk async
+ * group.  Four consumer warps update each stage; one producer thread loads.
+ *
+ *   src, dst  ATB_F32 maps with equal rank, box extents and swizzle
+ *             (ATB_ERR_DTYPE / ATB_ERR_ARG otherwise)
+ *   d_coords  as for atb_tile_load (NULL = the source's tile grid)
+ * Result = store(dst, coords, load(src, coords) + addend).  Elements outside
+ * the source read as 0 and are therefore stored as 0 + addend where they lie
+ * inside the destination.
+ */
+atb_status atb_tile_roundtrip_add_f32(const atb_tensor_map* src, const atb_tensor_map* dst,
+                                      const int32_t* d_coords, uint64_t n, float addend,
+                                      const atb_launch* launch, atb_stream_t stream);
 
 /*
  * Allocate this device's status block now (it is otherwise allocated on the

@@ -35,7 +35,7 @@ def build(force: bool = False) -> str:
     ):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC]
+            ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC]
         )
         os.replace(tmp, _LIB)
     return _LIB
@@ -76,6 +76,10 @@ def _load():
         lib.oracle_tile_store.restype = None
         lib.oracle_roundtrip.argtypes = [P, u8p, P, u8p, u8p, ctypes.c_uint64]
         lib.oracle_roundtrip.restype = ctypes.c_int32
+        lib.oracle_add_f32.argtypes = [u8p, ctypes.c_uint64, ctypes.c_float]
+        lib.oracle_add_f32.restype = None
+        lib.oracle_roundtrip_add_f32.argtypes = [P, u8p, P, u8p, u8p, ctypes.c_uint64, ctypes.c_float]
+        lib.oracle_roundtrip_add_f32.restype = ctypes.c_int32
         _lib = lib
     return _lib
 
@@ -179,3 +183,22 @@ def roundtrip(src: View, src_base: np.ndarray, dst: View, dst_base: np.ndarray, 
                                   _ptr(dst_base), _ptr(c), c.shape[0])
     if rc != 0:
         raise ValueError("oracle roundtrip: box shape, element size or swizzle differ, or out of memory")
+
+
+def add_f32(packed: np.ndarray, addend: float) -> np.ndarray:
+    """Copy of ``packed`` with ``addend`` added to every fp32 element."""
+    out = np.array(packed, dtype=np.uint8, copy=True)
+    _load().oracle_add_f32(_ptr(out), out.nbytes, float(addend))
+    return out
+
+
+def roundtrip_add_f32(src: View, src_base: np.ndarray, dst: View, dst_base: np.ndarray, coords: np.ndarray,
+                      addend: float) -> None:
+    """``store(dst, coords, load(src, coords) + addend)`` applied to ``dst_base`` in place."""
+    _check_base(src, src_base)
+    _check_base(dst, dst_base)
+    c = _coords(coords, src)
+    rc = _load().oracle_roundtrip_add_f32(ctypes.byref(src._c()), _ptr(src_base), ctypes.byref(dst._c()),
+                                          _ptr(dst_base), _ptr(c), c.shape[0], float(addend))
+    if rc != 0:
+        raise ValueError("oracle fp32 round trip: views differ, element size is not 4, or out of memory")

@@ -199,3 +199,40 @@ int32_t oracle_roundtrip(const oracle_view* src, const uint8_t* src_base,
     free(packed);
     return 0;
 }
+
+/*
+ * [D76] "An exact round trip": the page's kernel adds 1.0f to every element
+ * of the landed tile in shared memory; "Exercise"/"Solution" store the
+ * updated tile back with the tensor store.  Elementwise, so the swizzled
+ * order of the image does not matter.  Plain C float addition (binary32,
+ * round to nearest even, no contraction).
+ */
+void oracle_add_f32(uint8_t* packed, uint64_t bytes, float addend)
+{
+    for (uint64_t o = 0; o + 4 <= bytes; o += 4) {
+        float x;
+        memcpy(&x, packed + o, 4);
+        x = x + addend;
+        memcpy(packed + o, &x, 4);
+    }
+}
+
+int32_t oracle_roundtrip_add_f32(const oracle_view* src, const uint8_t* src_base,
+                                 const oracle_view* dst, uint8_t* dst_base,
+                                 const int32_t* coords, uint64_t n, float addend)
+{
+    if (src->esize != 4 || dst->esize != 4 || src->rank != dst->rank ||
+        src->swizzle_bits != dst->swizzle_bits)
+        return -1;
+    for (int32_t d = 0; d < src->rank; ++d)
+        if (src->box[d] != dst->box[d]) return -1;
+    uint64_t box_bytes = oracle_box_bytes(src);
+    if (n == 0) return 0;
+    uint8_t* packed = (uint8_t*)malloc(n * box_bytes);
+    if (!packed) return -1;
+    oracle_tile_load(src, src_base, coords, n, packed);
+    oracle_add_f32(packed, n * box_bytes, addend);
+    oracle_tile_store(dst, dst_base, coords, n, packed);
+    free(packed);
+    return 0;
+}

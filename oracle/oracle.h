@@ -63,6 +63,16 @@ int32_t oracle_roundtrip(const oracle_view* src, const uint8_t* src_base,
                          const oracle_view* dst, uint8_t* dst_base,
                          const int32_t* coords, uint64_t n);
 
+/* Adds `addend` to every fp32 element of `bytes` bytes of packed images, in
+ * place (IEEE binary32, round to nearest even). */
+void oracle_add_f32(uint8_t* packed, uint64_t bytes, float addend);
+
+/* store(dst, coords, load(src, coords) + addend) for fp32 views; returns 0,
+ * or -1 on mismatched views, a non-4-byte element or out of memory. */
+int32_t oracle_roundtrip_add_f32(const oracle_view* src, const uint8_t* src_base,
+                                 const oracle_view* dst, uint8_t* dst_base,
+                                 const int32_t* coords, uint64_t n, float addend);
+
 #ifdef __cplusplus
 }
 #endif

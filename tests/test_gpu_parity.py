@@ -363,3 +363,119 @@ def test_ablation_copies(atb, kind):
     {"cpasync": atb.copy_cpasync, "ldst_v4": atb.copy_ldst_v4, "memcpy": atb.copy_memcpy}[kind](src, dst, nbytes)
     device_ok(atb)
     assert_bytes_equal(host(dst), src_h, kind)
+
+
+# --------------------------------------------------------------------------
+# fp32 update in shared memory between load and store (generic-proxy writes,
+# fence.proxy.async, tensor store)
+# --------------------------------------------------------------------------
+def test_add_f32_day76_sixteen_tiles(atb):
+    v = oracle.View(4, (256, 256), (4, 1024), (64, 64))
+    src_h = datagen.finite_f32_bytes(256 * 256, 760)
+    src, dst = dev_bytes(src_h), dev_empty(256 * 1024, fill=0)
+    ms = atb.encode_tiled("f32", src, v.dims, v.strides, v.box)
+    md = atb.encode_tiled("f32", dst, v.dims, v.strides, v.box)
+    atb.tile_roundtrip_add_f32(ms, md, 1.0, ctas=16, stages=1)
+    device_ok(atb)
+    want = np.zeros_like(src_h)
+    oracle.roundtrip_add_f32(v, src_h, v, want, oracle.grid_coords(v), 1.0)
+    assert_bytes_equal(host(dst), want, "day76 +1.0f", view=v)
+
+
+@pytest.mark.parametrize("swizzle,box", [("none", (64, 16)), ("128B", (32, 16)), ("64B", (16, 8))])
+@pytest.mark.parametrize("launch", [dict(), dict(stages=1, ctas=1), dict(stages=4, ctas=7, store_groups=3)],
+                         ids=["default", "s1c1", "s4c7g3"])
+def test_add_f32_ragged_lists_and_grid(atb, swizzle, box, launch):
+    rows, cols = 300, 200
+    strides = (4, 816)  # padded rows
+    v = oracle.View(4, (cols, rows), strides, box, swizzle)
+    src_h = datagen.finite_f32_bytes(816 * rows // 4, 761)
+    coords_h = datagen.random_box_origins((cols, rows), box, 4, 257, 762)
+    src = dev_bytes(src_h)
+    coords = dev_bytes(coords_h.view(np.uint8))
+    ms = atb.encode_tiled("f32", src, (cols, rows), strides, box, swizzle)
+    for name, cl, nl in (("grid", None, 0), ("list", coords, len(coords_h))):
+        out = dev_empty(816 * rows, fill=0x7B)
+        md = atb.encode_tiled("f32", out, (cols, rows), strides, box, swizzle)
+        atb.tile_roundtrip_add_f32(ms, md, -0.75, cl, nl, **launch)
+        device_ok(atb)
+        want = np.full(816 * rows, 0x7B, dtype=np.uint8)
+        oracle.roundtrip_add_f32(v, src_h, v, want, oracle.grid_coords(v) if cl is None else coords_h, -0.75)
+        assert_bytes_equal(host(out), want, f"add_f32 {swizzle} {name}")
+
+
+def test_add_f32_full_size(atb):
+    # 16384 x 8192 fp32 (512 MiB), box 32x128 with 128B swizzle, library defaults
+    rows, cols = 8192, 16384
+    v = oracle.View(4, (cols, rows), (4, cols * 4), (32, 128), "128B")
+    src_h = datagen.finite_f32_bytes(rows * cols, 763)
+    src, dst = dev_bytes(src_h), dev_empty(rows * cols * 4, fill=0)
+    ms = atb.encode_tiled("f32", src, v.dims, v.strides, v.box, "128B")
+    md = atb.encode_tiled("f32", dst, v.dims, v.strides, v.box, "128B")
+    atb.tile_roundtrip_add_f32(ms, md, 1.0)
+    device_ok(atb)
+    want = np.zeros_like(src_h)
+    oracle.roundtrip_add_f32(v, src_h, v, want, oracle.grid_coords(v), 1.0)
+    assert_bytes_equal(host(dst), want, "add_f32 512 MiB", view=v)
+
+
+def test_add_f32_rejects_other_types(atb):
+    a = dev_empty(1 << 16)
+    m16 = atb.encode_tiled("f16", a, (256, 64), (2, 512), (64, 16))
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_roundtrip_add_f32(m16, m16, 1.0)
+    assert e.value.code == atb.ATB_ERR_DTYPE
+
+
+# --------------------------------------------------------------------------
+# host-resident round trip: slab-wise H2D copy, boxes, D2H copy on three streams
+# --------------------------------------------------------------------------
+HOST_CASES = [
+    # name, dtype, dims, strides, box, swizzle, slabs
+    ("padded_f16_5slabs", "f16", (1000, 777), (2, 2016), (64, 32), "none", 5),
+    ("nested_3d_f32_sw128", "f32", (64, 30, 17), (4, 272, 8160), (32, 8, 4), "128B", 4),
+    ("permuted_3d_one_slab", "f32", (64, 30, 17), (4, 4352, 256), (32, 8, 2), "128B", 3),
+    ("rank1_u8", "u8", (5000,), (1,), (64,), "none", 7),
+]
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=[c[0] for c in HOST_CASES])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_round_trip(atb, case, pinned):
+    torch = torch_cuda()
+    name, dtype, dims, strides, box, swizzle, slabs = case
+    esize = datagen.ESIZE[dtype]
+    v = oracle.View(esize, dims, strides, box, swizzle)
+    nbytes = ((v.span_bytes() + 15) // 16) * 16
+    src_h = datagen.random_bytes(nbytes, 800 + slabs)
+    dst_h = np.full(nbytes, 0x5A, dtype=np.uint8)
+    if pinned:
+        src_host = torch.from_numpy(src_h).pin_memory()
+        dst_host = torch.from_numpy(dst_h).pin_memory()
+    else:
+        src_host, dst_host = src_h.copy(), dst_h.copy()
+    d_src, d_dst = dev_empty(nbytes, fill=0), dev_empty(nbytes, fill=0x5A)
+    ms = atb.encode_tiled(dtype, d_src, dims, strides, box, swizzle)
+    md = atb.encode_tiled(dtype, d_dst, dims, strides, box, swizzle)
+    s = torch.cuda.Stream()
+    atb.tile_roundtrip_host(ms, md, src_host, dst_host, slabs, stream=s)
+    s.synchronize()
+    device_ok(atb)
+    got = dst_host.numpy() if pinned else dst_host
+    want = dst_h.copy()
+    oracle.roundtrip(v, src_h, v, want, oracle.grid_coords(v))
+    assert_bytes_equal(got, want, f"host round trip {name}")
+
+
+def test_host_round_trip_full_size(atb, c5_input):
+    torch = torch_cuda()
+    w = datagen.C5B
+    src_pin = torch.from_numpy(c5_input).pin_memory()
+    dst_pin = torch.zeros(w.storage_bytes, dtype=torch.uint8).pin_memory()
+    d_src, d_dst = dev_empty(w.storage_bytes), dev_empty(w.storage_bytes)
+    ms, md = encode(atb, w, d_src), encode(atb, w, d_dst)
+    atb.tile_roundtrip_host(ms, md, src_pin, dst_pin)
+    torch.cuda.synchronize()
+    device_ok(atb)
+    # the oracle's full-grid round trip reproduces its input (pinned on the CPU)
+    assert_bytes_equal(dst_pin.numpy(), c5_input, "host round trip 512 MiB", view=oracle_view(w))

@@ -322,3 +322,50 @@ def test_swapped_coordinates_load_transposed_positions():
     assert (right.view(np.uint32) != swapped.view(np.uint32)).mean() > 0.99
     a = buf.view(np.uint32).reshape(256, 256)
     np.testing.assert_array_equal(right.view(np.uint32).reshape(64, 64), a[128:192, 64:128])
+
+
+# --------------------------------------------------------------------------
+# fp32 update between load and store ("Day 76", +1.0f per element)
+# --------------------------------------------------------------------------
+def test_add_f32_closed_forms():
+    x = np.array([0.0, 1.5, -2.0, 2.0**24, 3.0e38, -0.0, 1e-45], dtype=np.float32)
+    got = oracle.add_f32(x.view(np.uint8), 1.0).view(np.float32)
+    np.testing.assert_array_equal(got[:3], np.array([1.0, 2.5, -1.0], dtype=np.float32))
+    assert got[3] == np.float32(2.0**24)        # 2^24 + 1 rounds to even: 2^24
+    assert got[4] == np.float32(3.0e38)         # absorbed
+    assert got[5] == 1.0 and got[6] == 1.0      # -0 + 1 and denormal + 1
+    z = oracle.add_f32(np.array([-0.0], dtype=np.float32).view(np.uint8), 0.0).view(np.uint32)
+    assert z[0] == 0                            # IEEE: -0 + +0 = +0
+
+
+def test_add_f32_matches_numpy_float32():
+    x = datagen.finite_f32_bytes(1 << 16, 8)
+    for addend in (1.0, -3.25, 1e-40, 6.5e37):
+        got = oracle.add_f32(x, addend).view(np.uint32)
+        with np.errstate(over="ignore"):  # finite + 6.5e37 may round to inf, as IEEE says
+            want = (x.view(np.float32) + np.float32(addend)).view(np.uint32)
+        np.testing.assert_array_equal(got, want)
+
+
+def test_roundtrip_add_f32_day76_matrix():
+    f = FACTS["day76_matrix"]
+    v = oracle.View(4, (256, 256), (4, 1024), (64, 64))
+    src = datagen.finite_f32_bytes(256 * 256, 76)
+    dst = np.zeros_like(src)
+    oracle.roundtrip_add_f32(v, src, v, dst, oracle.grid_coords(v), 1.0)
+    assert oracle.grid_count(v) == f["tiles"]
+    want = (src.view(np.float32) + np.float32(1.0)).view(np.uint8)
+    np.testing.assert_array_equal(dst, want)
+
+
+def test_roundtrip_add_f32_edges_get_addend_where_source_is_outside():
+    # destination larger than the source: its extra elements read source zeros
+    vs = oracle.View(4, (20, 10), (4, 80), (16, 4))
+    vd = oracle.View(4, (32, 12), (4, 128), (16, 4))
+    src = datagen.finite_f32_bytes(200, 9)
+    dst = np.full(12 * 128, 0xCD, dtype=np.uint8)
+    oracle.roundtrip_add_f32(vs, src, vd, dst, oracle.grid_coords(vd), 2.0)
+    d = dst.view(np.float32).reshape(12, 32)
+    s = src.view(np.float32).reshape(10, 20)
+    np.testing.assert_array_equal(d[:10, :20], s + np.float32(2.0))
+    assert (d[:12, 20:32] == 2.0).all() and (d[10:12, :20] == 2.0).all()
