@@ -50,6 +50,7 @@ class _View(ctypes.Structure):
         ("dims", ctypes.c_uint64 * MAX_RANK),
         ("strides", ctypes.c_uint64 * MAX_RANK),
         ("box", ctypes.c_uint32 * MAX_RANK),
+        ("estr", ctypes.c_uint32 * MAX_RANK),
     ]
 
 
@@ -97,6 +98,7 @@ class View:
     strides: tuple
     box: tuple
     swizzle: str = "none"
+    estr: tuple | None = None  # traversal steps per dimension (None = all 1)
     rank: int = field(init=False)
 
     def __post_init__(self):
@@ -104,6 +106,7 @@ class View:
         assert 1 <= self.rank <= MAX_RANK
         assert len(self.strides) == self.rank and len(self.box) == self.rank
         assert self.strides[0] == self.esize
+        assert self.estr is None or (len(self.estr) == self.rank and self.estr[0] == 1)
 
     def _c(self) -> _View:
         v = _View()
@@ -114,6 +117,7 @@ class View:
             v.dims[d] = int(self.dims[d])
             v.strides[d] = int(self.strides[d])
             v.box[d] = int(self.box[d])
+            v.estr[d] = int(self.estr[d]) if self.estr is not None else 1
         return v
 
     def span_bytes(self) -> int:

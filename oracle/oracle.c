@@ -27,6 +27,9 @@
  *   R4  the packed buffer holds box i at byte offset i*box_bytes, in the order
  *       of the coordinate list; the full tile grid is enumerated row-major over
  *       tile indices, innermost tile index fastest.
+ *   R5  a traversal step e along an outer dimension makes the box visit every
+ *       e-th element of its extent (ceil(box / e) elements), packed densely in
+ *       the image; the tile grid still advances by the box extent.
  *
  * Parity of every function is pinned by tests that do not re-type these
  * formulas: the byte counts and tile positions the pages print, brute-force
@@ -57,12 +60,27 @@ uint64_t oracle_swizzle(uint64_t offset, int32_t bits)
     return offset ^ ((offset & source_mask) >> S);
 }
 
+/* Traversal step along dimension d (1 when unset).  Reading R5: a box with
+ * step e along d visits elements origin, origin + e, ... inside its extent,
+ * ceil(box / e) of them; the innermost dimension is always contiguous. */
+static uint64_t step_along(const oracle_view* v, int32_t d)
+{
+    return v->estr[d] > 1 ? v->estr[d] : 1;
+}
+
+/* Elements the box visits along dimension d. */
+static uint64_t visits_along(const oracle_view* v, int32_t d)
+{
+    return (v->box[d] + step_along(v, d) - 1) / step_along(v, d);
+}
+
 /* [D76] "The address arithmetic moves into a descriptor": a 64x64 float box
- * is a 16384-byte transfer; the box size is the product of its extents. */
+ * is a 16384-byte transfer; the box size is the product of its extents (of
+ * the visited elements when a traversal step is set). */
 uint64_t oracle_box_bytes(const oracle_view* v)
 {
     uint64_t elems = 1;
-    for (int32_t d = 0; d < v->rank; ++d) elems *= v->box[d];
+    for (int32_t d = 0; d < v->rank; ++d) elems *= visits_along(v, d);
     return elems * (uint64_t)v->esize;
 }
 
@@ -112,9 +130,9 @@ static int element_in_bounds(const oracle_view* v, const int32_t* c, uint64_t e,
     uint64_t rest = e;
     int inside = 1;
     for (int32_t d = 0; d < v->rank; ++d) {
-        int64_t k = (int64_t)(rest % v->box[d]);
-        rest /= v->box[d];
-        g[d] = (int64_t)c[d] + k;
+        int64_t k = (int64_t)(rest % visits_along(v, d));
+        rest /= visits_along(v, d);
+        g[d] = (int64_t)c[d] + k * (int64_t)step_along(v, d);
         if (g[d] < 0 || g[d] >= (int64_t)v->dims[d]) inside = 0;
     }
     return inside;
@@ -189,7 +207,7 @@ int32_t oracle_roundtrip(const oracle_view* src, const uint8_t* src_base,
         src->swizzle_bits != dst->swizzle_bits)
         return -1;
     for (int32_t d = 0; d < src->rank; ++d)
-        if (src->box[d] != dst->box[d]) return -1;
+        if (src->box[d] != dst->box[d] || step_along(src, d) != step_along(dst, d)) return -1;
     uint64_t box_bytes = oracle_box_bytes(src);
     if (n == 0) return 0;
     uint8_t* packed = (uint8_t*)malloc(n * box_bytes);
@@ -225,7 +243,7 @@ int32_t oracle_roundtrip_add_f32(const oracle_view* src, const uint8_t* src_base
         src->swizzle_bits != dst->swizzle_bits)
         return -1;
     for (int32_t d = 0; d < src->rank; ++d)
-        if (src->box[d] != dst->box[d]) return -1;
+        if (src->box[d] != dst->box[d] || step_along(src, d) != step_along(dst, d)) return -1;
     uint64_t box_bytes = oracle_box_bytes(src);
     if (n == 0) return 0;
     uint8_t* packed = (uint8_t*)malloc(n * box_bytes);

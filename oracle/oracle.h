@@ -35,12 +35,14 @@ typedef struct {
     uint64_t dims[ORACLE_MAX_RANK];     /* extent per dimension, innermost first */
     uint64_t strides[ORACLE_MAX_RANK];  /* byte stride per dimension, innermost first */
     uint32_t box[ORACLE_MAX_RANK];      /* box extent per dimension, innermost first */
+    uint32_t estr[ORACLE_MAX_RANK];     /* traversal step per dimension (0 or 1 = every element) */
 } oracle_view;
 
 /* Swizzle<B,4,3> applied to a byte offset inside a box image. */
 uint64_t oracle_swizzle(uint64_t offset, int32_t bits);
 
-/* Bytes of one box: product of the box extents times the element size. */
+/* Bytes of one box image: the element size times, per dimension, the number
+ * of elements the box visits (ceil(box / step)). */
 uint64_t oracle_box_bytes(const oracle_view* v);
 
 /* Number of boxes that tile the whole tensor (edge boxes included). */

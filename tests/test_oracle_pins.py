@@ -369,3 +369,72 @@ def test_roundtrip_add_f32_edges_get_addend_where_source_is_outside():
     s = src.view(np.float32).reshape(10, 20)
     np.testing.assert_array_equal(d[:10, :20], s + np.float32(2.0))
     assert (d[:12, 20:32] == 2.0).all() and (d[10:12, :20] == 2.0).all()
+
+
+# --------------------------------------------------------------------------
+# traversal steps (elementStrides): every e-th element along outer dimensions
+# --------------------------------------------------------------------------
+def np_box_stepped(buf, v, origin):
+    """Box with traversal steps by numpy: zero-pad, then slice with a step."""
+    a = np_view(buf, v)
+    c = [int(x) for x in reversed(origin)]
+    b = [int(x) for x in reversed(v.box)]
+    e = [int(x) for x in reversed(v.estr)]
+    n = [int(x) for x in reversed(v.dims)]
+    pads = [(max(0, -ci), max(0, ci + bi - ni)) for ci, bi, ni in zip(c, b, n)]
+    p = np.pad(a, pads + [(0, 0)])
+    sl = tuple(slice(ci + lo, ci + lo + bi, ei) for ci, bi, ei, (lo, _) in zip(c, b, e, pads))
+    return p[sl]
+
+
+def test_box_bytes_with_traversal_steps():
+    v = oracle.View(2, (64, 40, 9), (2, 128, 5120), (64, 8, 3), "none", (1, 2, 3))
+    assert oracle.box_bytes(v) == 64 * 4 * 1 * 2
+    v = oracle.View(4, (64, 40), (4, 256), (32, 7), "128B", (1, 3))
+    assert oracle.box_bytes(v) == 32 * 3 * 4  # ceil(7 / 3) = 3 visits
+
+
+@pytest.mark.parametrize("steps", [(1, 2), (1, 3), (1, 8)])
+def test_gather_with_traversal_steps_brute_force(steps):
+    rows, cols, esize = 23, 40, 2
+    v = oracle.View(esize, (cols, rows), (esize, cols * esize + 16), (16, 9), "none", steps)
+    buf = datagen.random_bytes(v.span_bytes() + 32, 91)
+    origins = np.array([(x, y) for y in range(-9, 24, 4) for x in range(-16, 41, 8)], dtype=np.int32)
+    packed = oracle.tile_load(v, buf, origins)
+    bb = oracle.box_bytes(v)
+    for i, o in enumerate(origins):
+        np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], np_box_stepped(buf, v, o).reshape(-1),
+                                      err_msg=f"origin {o}")
+
+
+def test_gather_3d_steps_and_swizzle():
+    esize = 4
+    dims, box, steps = (32, 11, 13), (32, 5, 6), (1, 2, 4)
+    strides = (4, 128 + 16, (128 + 16) * 11)
+    v = oracle.View(esize, dims, strides, box, "128B", steps)
+    buf = datagen.random_bytes(v.span_bytes() + 16, 92)
+    g = datagen.rng(3)
+    origins = np.stack([g.integers(-1, 2, 50) * 32, g.integers(-4, 11, 50), g.integers(-5, 13, 50)], 1).astype(np.int32)
+    packed = oracle.tile_load(v, buf, origins)
+    bb = oracle.box_bytes(v)
+    for i, o in enumerate(origins):
+        want = swizzle_image(np_box_stepped(buf, v, o).reshape(-1), "128B")
+        np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], want)
+
+
+def test_store_with_steps_writes_only_visited_elements():
+    rows, cols = 17, 32
+    v = oracle.View(4, (cols, rows), (4, 128), (32, 8), "none", (1, 3))
+    base = np.full(rows * 128, 0x11, dtype=np.uint8)
+    origins = np.array([[0, 0], [0, 8], [0, 16]], dtype=np.int32)
+    packed = datagen.random_bytes(3 * oracle.box_bytes(v), 93)
+    oracle.tile_store(v, base, origins, packed)
+    a = base.view(np.uint32).reshape(rows, cols)
+    img = packed.view(np.uint32).reshape(3, 3, 32)  # ceil(8 / 3) = 3 rows per box
+    for i, y0 in enumerate((0, 8, 16)):
+        for k in range(3):
+            y = y0 + 3 * k
+            if y < rows:
+                np.testing.assert_array_equal(a[y], img[i, k])
+    untouched = [y for y in range(rows) if (y % 8) % 3 != 0 or (y % 8) > 6]
+    assert (base.reshape(rows, 128)[untouched] == 0x11).all()
