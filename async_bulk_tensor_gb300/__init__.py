@@ -53,6 +53,7 @@ class TensorMap(ctypes.Structure):
         ("dims", ctypes.c_uint64 * MAX_RANK),
         ("strides", ctypes.c_uint64 * MAX_RANK),
         ("box", ctypes.c_uint32 * MAX_RANK),
+        ("elem_strides", ctypes.c_uint32 * MAX_RANK),
         ("rank", ctypes.c_uint32),
         ("esize", ctypes.c_uint32),
         ("dtype", ctypes.c_uint32),
@@ -76,6 +77,8 @@ class Launch(ctypes.Structure):
         ("l2_hints", ctypes.c_uint32),
         ("no_pdl", ctypes.c_uint32),
         ("poll_suspend_ns", ctypes.c_uint32),
+        ("prefetch_boxes", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32 * 3),
     ]
 
 
@@ -167,9 +170,9 @@ HINT_LOAD_EVICT_FIRST, HINT_STORE_EVICT_FIRST, HINT_STORE_EVICT_LAST = 1, 2, 4
 
 
 def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True,
-            poll_suspend_ns=0) -> Launch:
+            poll_suspend_ns=0, prefetch_boxes=0) -> Launch:
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
-                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns)
+                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes)
 
 
 def version() -> int:

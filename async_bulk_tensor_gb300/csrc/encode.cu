@@ -254,17 +254,23 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
     if (span_bytes && inner_bytes != span_bytes)
         return set_error(ATB_ERR_SWIZZLE_SPAN, "inner box bytes %llu must equal the %u-byte swizzle span",
                          static_cast<unsigned long long>(inner_bytes), span_bytes);
-    if (elem_strides)
-        for (uint32_t d = 0; d < rank; ++d)
-            if (elem_strides[d] != 1)
-                return set_error(ATB_ERR_ARG, "elem_strides[%u] = %u; only unit traversal strides are supported", d,
-                                 elem_strides[d]);
+    uint32_t steps[ATB_MAX_RANK] = {1, 1, 1, 1, 1};
+    if (elem_strides) {
+        if (elem_strides[0] != 1)
+            return set_error(ATB_ERR_ARG, "elem_strides[0] = %u; the innermost traversal step must be 1",
+                             elem_strides[0]);
+        for (uint32_t d = 1; d < rank; ++d) {
+            if (elem_strides[d] < 1 || elem_strides[d] > 8)
+                return set_error(ATB_ERR_ARG, "elem_strides[%u] = %u is outside 1..8", d, elem_strides[d]);
+            steps[d] = elem_strides[d];
+        }
+    }
     if (static_cast<uint32_t>(l2_promotion) > ATB_L2_PROMO_256B)
         return set_error(ATB_ERR_ARG, "unknown L2 promotion %d", static_cast<int>(l2_promotion));
     if (oob_fill != ATB_OOB_ZERO) return set_error(ATB_ERR_ARG, "only zero out-of-bounds fill is supported");
 
     uint64_t box_bytes = esize;
-    for (uint32_t d = 0; d < rank; ++d) box_bytes *= box[d];
+    for (uint32_t d = 0; d < rank; ++d) box_bytes *= (box[d] + steps[d] - 1) / steps[d];
     if (box_bytes > 0xFFFFFFFFull) return set_error(ATB_ERR_BOX_DIM, "box of %llu bytes is too large",
                                                     static_cast<unsigned long long>(box_bytes));
 
@@ -279,7 +285,7 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
     for (uint32_t d = 0; d < rank; ++d) {
         gdim[d] = dims[d];
         bdim[d] = box[d];
-        estr[d] = 1;
+        estr[d] = steps[d];
         if (d + 1 < rank) gstride[d] = strides_bytes[d + 1];
     }
     alignas(64) CUtensorMap map;
@@ -296,6 +302,7 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
         out->dims[d] = dims[d];
         out->strides[d] = d == 0 ? esize : strides_bytes[d];
         out->box[d] = box[d];
+        out->elem_strides[d] = steps[d];
     }
     out->rank = rank;
     out->esize = esize;

@@ -52,6 +52,8 @@ struct PipeArgs {
     uint64_t dst_strides[ATB_MAX_RANK];
     uint32_t grid[ATB_MAX_RANK];  // boxes along each dimension (tile grid)
     uint32_t box[ATB_MAX_RANK];
+    uint32_t visits[ATB_MAX_RANK];  // elements a box visits per dimension: ceil(box / step)
+    uint32_t step[ATB_MAX_RANK];    // traversal step per dimension
     uint32_t n_tiles;       // boxes in this launch
     uint32_t tile_begin;    // index of its first box in the list or grid
     uint32_t esize;
@@ -64,6 +66,7 @@ struct PipeArgs {
     uint32_t dst_ragged_x;  // destination rows end inside a 16-byte chunk
     uint32_t l2_hints;      // ATB_HINT_* bits
     uint32_t suspend_ns;    // mbarrier poll suspend-time hint, 0 = hardware default
+    uint32_t prefetch;      // boxes ahead to prefetch into L2 (tensor loads), 0 = off
 };
 
 // Shared-memory control words after the stage ring and the barriers.
@@ -197,7 +200,7 @@ template <int R>
 __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], const uint8_t* stage, uint32_t tid,
                                 uint32_t nthreads)
 {
-    const uint32_t row_bytes = a.box[0] * a.esize;
+    const uint32_t row_bytes = a.box[0] * a.esize;  // the innermost step is always 1
     const uint32_t chunks_per_row = row_bytes / 16;
     const uint32_t rows = a.box_bytes / row_bytes;
     const uint32_t q = 16 / a.esize;  // elements per chunk
@@ -210,9 +213,9 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], const 
         uint64_t addr = 0;
 #pragma unroll
         for (int d = 1; d < R; ++d) {
-            const uint32_t k = rest % a.box[d];
-            rest /= a.box[d];
-            const int64_t g = static_cast<int64_t>(c[d]) + k;
+            const uint32_t k = rest % a.visits[d];
+            rest /= a.visits[d];
+            const int64_t g = static_cast<int64_t>(c[d]) + static_cast<int64_t>(k) * a.step[d];
             if (g < 0 || g >= static_cast<int64_t>(a.dst_dims[d])) inside = false;
             else addr += static_cast<uint64_t>(g) * a.dst_strides[d];
         }
@@ -292,8 +295,20 @@ __device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, con
     const bool hint = (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
     const uint64_t policy = hint ? ptx::policy_evict_first() : 0;
     const uint32_t S = r.stages;
+    if (MODE != kStore && a.prefetch) {  // warm L2 with the first boxes
+        for (uint32_t k = 0; k < a.prefetch && k < count; ++k) {
+            int32_t c[R];
+            tile_origin<R>(a, tile_of(a, k), c);
+            if (!origin_error<R>(a, c)) ptx::tma_prefetch_l2<R>(&src_map, c);
+        }
+    }
     for (uint32_t k = 0; k < count; ++k) {
         const uint32_t s = k % S, use = k / S;
+        if (MODE != kStore && a.prefetch && k + a.prefetch < count) {
+            int32_t c[R];
+            tile_origin<R>(a, tile_of(a, k + a.prefetch), c);
+            if (!origin_error<R>(a, c)) ptx::tma_prefetch_l2<R>(&src_map, c);
+        }
         if (k >= S && !wait_bounded(r.empty(s), (use - 1) & 1, a.timeout_ns, r.abort_flag(), a.suspend_ns)) {
             raise_abort(a, r, tile_of(a, k), kWhereProducerWait);
             break;
@@ -596,10 +611,11 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
                          dst->dtype);
     if (MODE == kRoundtrip || MODE == kRoundtripAddF32) {
         bool same = src->rank == dst->rank && src->esize == dst->esize && src->swizzle == dst->swizzle;
-        for (uint32_t d = 0; same && d < src->rank; ++d) same = src->box[d] == dst->box[d];
+        for (uint32_t d = 0; same && d < src->rank; ++d)
+            same = src->box[d] == dst->box[d] && src->elem_strides[d] == dst->elem_strides[d];
         if (!same)
             return set_error(ATB_ERR_ARG,
-                             "source and destination maps differ in rank, element size, box or swizzle");
+                             "source and destination maps differ in rank, element size, box, steps or swizzle");
     }
     if (MODE == kLoad || MODE == kStore) {
         if (!packed) return set_error(ATB_ERR_ARG, "packed buffer is NULL");
@@ -678,9 +694,12 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.contiguous = cfg && cfg->schedule == 1 ? 1u : 0u;
     a.l2_hints = cfg ? cfg->l2_hints : 0u;
     a.suspend_ns = cfg ? cfg->poll_suspend_ns : 0u;
+    a.prefetch = cfg ? cfg->prefetch_boxes : 0u;
     a.swizzle_bits = swizzle_bits(shape->swizzle);
     for (uint32_t d = 0; d < rank; ++d) {
         a.box[d] = shape->box[d];
+        a.step[d] = shape->elem_strides[d] ? shape->elem_strides[d] : 1;
+        a.visits[d] = (shape->box[d] + a.step[d] - 1) / a.step[d];
         a.grid[d] = static_cast<uint32_t>((shape->dims[d] + shape->box[d] - 1) / shape->box[d]);
     }
     if (MODE != kLoad) {  // every mode that writes a tensor

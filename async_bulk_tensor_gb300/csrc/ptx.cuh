@@ -355,6 +355,50 @@ __device__ __forceinline__ void tma_store_hint<5>(const void* map, const int32_t
         : "memory");
 }
 
+// Brings a box into L2 ahead of its load; no completion to wait for.
+template <int R>
+__device__ __forceinline__ void tma_prefetch_l2(const void* map, const int32_t* c);
+template <>
+__device__ __forceinline__ void tma_prefetch_l2<1>(const void* map, const int32_t* c)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.1d.L2.global.tile [%0, {%1}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0])
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_prefetch_l2<2>(const void* map, const int32_t* c)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0]), "r"(c[1])
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_prefetch_l2<3>(const void* map, const int32_t* c)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0]), "r"(c[1]), "r"(c[2])
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_prefetch_l2<4>(const void* map, const int32_t* c)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3])
+                 : "memory");
+}
+template <>
+__device__ __forceinline__ void tma_prefetch_l2<5>(const void* map, const int32_t* c)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
+                 : "memory");
+}
+
 // ---- 1-D bulk copies (contiguous byte ranges, 16-byte aligned, size % 16 == 0)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
 {

@@ -398,6 +398,9 @@ def workload_lines(torch, atb, datagen, device, stream, args):
     inb = box_inbound_bytes(w.dims, w.box, w.esize, coords_h)
     warm, cold = timed(lambda: atb.tile_load(ms, coords, n, packed, stream=stream), 500, 30)
     out[w.name + "_load"] = line(inb + n * bb, n, warm, cold)
+    for pf in (4, 16):
+        warm, cold = timed(lambda: atb.tile_load(ms, coords, n, packed, stream=stream, prefetch_boxes=pf), 500, 30)
+        out[w.name + f"_load_prefetch{pf}"] = line(inb + n * bb, n, warm, cold)
     warm, cold = timed(lambda: atb.tile_store(mf, coords, n, packed, stream=stream), 500, 30)
     out[w.name + "_store"] = line(n * bb + inb, n, warm, cold)
     atb.check_device(stream)

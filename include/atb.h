@@ -111,13 +111,14 @@ typedef struct {
     uint64_t dims[ATB_MAX_RANK];      /* innermost first */
     uint64_t strides[ATB_MAX_RANK];   /* byte strides; strides[0] = element size */
     uint32_t box[ATB_MAX_RANK];       /* innermost first */
+    uint32_t elem_strides[ATB_MAX_RANK]; /* traversal step per dimension; [0] = 1 */
     uint32_t rank;
     uint32_t esize;                   /* element size in bytes */
     uint32_t dtype;                   /* atb_dtype */
     uint32_t swizzle;                 /* atb_swizzle */
     uint32_t l2_promotion;            /* atb_l2_promotion */
     uint32_t oob_fill;                /* atb_oob_fill */
-    uint32_t box_bytes;               /* product of box extents x element size */
+    uint32_t box_bytes;               /* element size x product over d of ceil(box[d] / elem_strides[d]) */
     uint32_t magic;                   /* set by atb_encode_tiled */
 } atb_tensor_map;
 
@@ -133,6 +134,9 @@ typedef struct {
     uint32_t l2_hints;     /* ATB_HINT_* bits: L2 eviction policy of the box loads and stores */
     uint32_t no_pdl;       /* 1 = launch without programmatic dependent launch (see below) */
     uint32_t poll_suspend_ns; /* mbarrier waits: suspend-time hint per poll in ns (0 = hardware default) */
+    uint32_t prefetch_boxes;  /* tensor loads: prefetch the box this many boxes ahead into L2 with
+                                 cp.async.bulk.prefetch.tensor (0 = off) */
+    uint32_t reserved[3];
 } atb_launch;
 
 /* atb_launch.l2_hints bits */
@@ -185,7 +189,7 @@ const char* atb_last_error(void);
  *   box[0] * element size multiple of 16         -> ATB_ERR_INNER_BYTES
  *   swizzle known                                -> ATB_ERR_SWIZZLE
  *   swizzled: box[0] * element size == span (32/64/128) -> ATB_ERR_SWIZZLE_SPAN
- *   elem_strides NULL or all 1                   -> ATB_ERR_ARG
+ *   elem_strides NULL, or [0] == 1 and each entry in 1..8 -> ATB_ERR_ARG
  * then fetches cuTensorMapEncodeTiled through the runtime's driver entry point
  * (no libcuda link) and encodes; a driver refusal -> ATB_ERR_DRIVER.
  *
@@ -197,7 +201,12 @@ const char* atb_last_error(void);
  *                 distance between neighbours along dimension d; NULL is not
  *                 allowed for rank > 1
  *   box           rank box extents, innermost first
- *   elem_strides  NULL, or rank entries that must all be 1
+ *   elem_strides  NULL (all 1), or rank traversal steps: along dimension d
+ *                 the box visits elements origin, origin + e, ... inside its
+ *                 extent, ceil(box[d] / e) of them, packed densely in the
+ *                 image (the driver's elementStrides).  The innermost step
+ *                 must be 1 (the engine has no step along the contiguous
+ *                 dimension).  The tile grid still advances by box[d].
  */
 atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank, void* gbase,
                             const uint64_t* dims, const uint64_t* strides_bytes,
@@ -205,7 +214,7 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
                             atb_swizzle swizzle, atb_l2_promotion l2_promotion,
                             atb_oob_fill oob_fill);
 
-/* Box bytes of a map (product of the box extents x element size); 0 if map is NULL. */
+/* Bytes of one box image of a map (see atb_tensor_map.box_bytes); 0 if map is NULL. */
 size_t atb_box_bytes(const atb_tensor_map* map);
 
 /* Number of boxes that tile the whole tensor, edge boxes included; 0 if map is NULL. */

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(atb):
 
 def test_struct_layouts(atb):
     assert atb.lib.atb_tensor_map_size() == ctypes.sizeof(atb.TensorMap)
-    assert ctypes.sizeof(atb.Launch) == 32
+    assert ctypes.sizeof(atb.Launch) == 48
     assert ctypes.sizeof(atb.DeviceReport) == 32
 
 
@@ -81,7 +81,9 @@ def test_encoder_rules_each_have_their_own_status(atb):
     _expect(atb, atb.ATB_ERR_SWIZZLE, swizzle=9)
     _expect(atb, atb.ATB_ERR_SWIZZLE_SPAN, box=(32, 16), swizzle="128B")  # 64 bytes != 128
     _expect(atb, atb.ATB_ERR_SWIZZLE_SPAN, box=(64, 16), swizzle="32B")
-    _expect(atb, atb.ATB_ERR_ARG, elem_strides=(1, 2))
+    _expect(atb, atb.ATB_ERR_ARG, elem_strides=(2, 1))  # no step along the contiguous dimension
+    _expect(atb, atb.ATB_ERR_ARG, elem_strides=(1, 9))  # steps are 1..8
+    _expect(atb, atb.ATB_ERR_ARG, elem_strides=(1, 0))
 
 
 def test_valid_map_reaches_the_driver(atb):

@@ -109,6 +109,10 @@ def test_c4_permuted_view_random_gather_then_store(atb):
     v = oracle_view(w)
     want_packed = oracle.tile_load(v, src_h, coords_h)
     assert_bytes_equal(host(packed), want_packed, "c4 gather", image_bytes=bb)
+    packed_pf = dev_empty(n * bb, fill=0xEE)
+    atb.tile_load(ms, coords, n, packed_pf, prefetch_boxes=8)
+    device_ok(atb)
+    assert_bytes_equal(host(packed_pf), want_packed, "c4 gather with L2 prefetch", image_bytes=bb)
 
     fresh = dev_empty(w.storage_bytes, fill=0xFF)
     md = encode(atb, w, fresh)
@@ -213,8 +217,9 @@ def _small_case(name, dtype, dims, box, swizzle, order, seed):
 
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 @pytest.mark.parametrize("launch", [dict(stages=1, ctas=1), dict(stages=3, ctas=5, store_groups=2),
-                                    dict(stages=2, ctas=3, schedule="contiguous"), dict()],
-                         ids=["s1c1", "s3c5g2", "s2c3contig", "default"])
+                                    dict(stages=2, ctas=3, schedule="contiguous"), dict(),
+                                    dict(prefetch_boxes=3, l2_hints=3, poll_suspend_ns=20000)],
+                         ids=["s1c1", "s3c5g2", "s2c3contig", "default", "prefetch3_hints"])
 def test_small_cases_all_ops(atb, case, launch):
     name, dtype, dims, box, swizzle, order = case
     v, src_h, nbytes, coords_h = _small_case(name, dtype, dims, box, swizzle, order, 1000 + len(name))
@@ -479,3 +484,77 @@ def test_host_round_trip_full_size(atb, c5_input):
     device_ok(atb)
     # the oracle's full-grid round trip reproduces its input (pinned on the CPU)
     assert_bytes_equal(dst_pin.numpy(), c5_input, "host round trip 512 MiB", view=oracle_view(w))
+
+
+# --------------------------------------------------------------------------
+# traversal steps (elementStrides): every e-th element along outer dimensions
+# --------------------------------------------------------------------------
+STEP_CASES = [
+    # name, dtype, dims, box, swizzle, steps
+    ("f16_2d_step2", "f16", (300, 90), (64, 16), "none", (1, 2)),
+    ("f32_2d_step3_sw128", "f32", (200, 77), (32, 10), "128B", (1, 3)),
+    ("u8_3d_steps_sw64", "u8", (256, 20, 15), (64, 6, 4), "64B", (1, 2, 4)),
+    ("bf16_4d_step8", "bf16", (64, 5, 33, 3), (32, 2, 16, 2), "64B", (1, 1, 8, 2)),
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=[c[0] for c in STEP_CASES])
+def test_traversal_steps_all_ops(atb, case):
+    name, dtype, dims, box, swizzle, steps = case
+    esize = datagen.ESIZE[dtype]
+    strides, nbytes = _strides(esize, dims)
+    v = oracle.View(esize, dims, strides, box, swizzle, steps)
+    src_h = datagen.random_bytes(nbytes, 900 + len(name))
+    coords_h = datagen.random_box_origins(dims, box, esize, 61, 901)
+    src = dev_bytes(src_h)
+    coords = dev_bytes(coords_h.view(np.uint8))
+    ms = atb.encode_tiled(dtype, src, dims, strides, box, swizzle, elem_strides=steps)
+    bb = atb.box_bytes(ms)
+    assert bb == oracle.box_bytes(v)
+    n = len(coords_h)
+    packed = dev_empty(n * bb, fill=0xEE)
+    atb.tile_load(ms, coords, n, packed)
+    device_ok(atb)
+    want_packed = oracle.tile_load(v, src_h, coords_h)
+    assert_bytes_equal(host(packed), want_packed, f"{name} load", image_bytes=bb)
+
+    grid_h = oracle.grid_coords(v)
+    images_h = datagen.random_bytes(len(grid_h) * bb, 902)
+    out = dev_empty(nbytes, fill=0x5A)
+    md = atb.encode_tiled(dtype, out, dims, strides, box, swizzle, elem_strides=steps)
+    atb.tile_store(md, None, 0, dev_bytes(images_h))
+    device_ok(atb)
+    want = np.full(nbytes, 0x5A, dtype=np.uint8)
+    oracle.tile_store(v, want, grid_h, images_h)
+    assert_bytes_equal(host(out), want, f"{name} grid store")
+
+    out2 = dev_empty(nbytes, fill=0x33)
+    md2 = atb.encode_tiled(dtype, out2, dims, strides, box, swizzle, elem_strides=steps)
+    atb.tile_roundtrip(ms, md2, coords, n)
+    device_ok(atb)
+    want2 = np.full(nbytes, 0x33, dtype=np.uint8)
+    oracle.roundtrip(v, src_h, v, want2, coords_h)
+    assert_bytes_equal(host(out2), want2, f"{name} listed round trip")
+
+
+def test_tensor_larger_than_4gib(atb):
+    # fp16 36864 x 65536 (4.5 GiB): 64-bit offsets end to end; every byte by the
+    # round-trip property (the oracle's full-grid round trip is the identity, pinned
+    # on the CPU), 48 sampled boxes by the oracle itself
+    torch = torch_cuda()
+    rows, cols = 36864, 65536
+    nbytes = rows * cols * 2
+    v = oracle.View(2, (cols, rows), (2, cols * 2), (64, 128), "128B")
+    src_h = datagen.random_bytes(nbytes, 4096)
+    src, dst = dev_bytes(src_h), dev_empty(nbytes, fill=0)
+    ms = atb.encode_tiled("f16", src, v.dims, v.strides, v.box, "128B")
+    md = atb.encode_tiled("f16", dst, v.dims, v.strides, v.box, "128B")
+    atb.tile_roundtrip(ms, md)
+    device_ok(atb)
+    assert torch.equal(src, dst)
+    dst_h = host(dst)
+    g = datagen.rng(4097)
+    sample = np.stack([g.integers(0, cols // 64, 48) * 64, g.integers(0, rows // 128, 48) * 128], 1).astype(np.int32)
+    sample[-1] = (cols - 64, rows - 128)  # the box with the largest offsets
+    assert_bytes_equal(oracle.tile_load(v, dst_h, sample), oracle.tile_load(v, src_h, sample), "4.5 GiB sampled",
+                       image_bytes=oracle.box_bytes(v))
