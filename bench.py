@@ -174,7 +174,7 @@ def committed_traffic():
         return None, "summary lacks traffic or source hash"
     if h.group(1) != kernel_source_hash():
         return None, "kernel changed since the ncu capture"
-    return int(m.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum, scaled per launch"
+    return int(m.group(1)), "ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch"
 
 
 # ---------------------------------------------------------------------------
@@ -217,7 +217,7 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=device)
 
     w = datagen.C5A if args.box == "64x256" else datagen.C5B
-    launch = dict(stages=args.stages, ctas_per_sm=args.ctas_per_sm)
+    launch = dict(stages=args.stages, ctas_per_sm=args.ctas_per_sm, poll_suspend_ns=args.poll_suspend_ns)
     src_h = datagen.storage(w)
     nbytes = w.storage_bytes
     src = torch.from_numpy(src_h).to(device)
@@ -512,6 +512,7 @@ def main(argv=None):
     p.add_argument("--box", choices=["64x256", "128x64"], default="128x64")
     p.add_argument("--stages", type=int, default=0, help="0 = library default")
     p.add_argument("--ctas-per-sm", type=int, default=0, help="0 = library default")
+    p.add_argument("--poll-suspend-ns", type=int, default=0, help="mbarrier poll suspend hint (0 = default)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--slabs", type=int, default=0, help="host round trip slabs (0 = library default)")
     p.add_argument("--ref-tiles", type=int, default=1024, help="boxes per reference-arm step")
