@@ -90,14 +90,18 @@ __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int
 // Waits for the phase of `bar` with the given parity for at most `timeout_ns`.
 // Returns false on expiry or, when `abort` is non-null, once another role
 // has raised it.  The timer is read only after the first poll fails.
+// Each poll may suspend the thread until the phase completes (for a
+// hardware-chosen time, or at most `suspend_ns` when that is non-zero).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                              const volatile uint32_t* abort, uint32_t suspend_ns = 0)
 {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() {
+        return suspend_ns ? ptx::mbar_try_wait_suspend(bar, parity, suspend_ns) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
     const uint64_t t0 = ptx::global_timer_ns();
     for (;;) {
-        if (suspend_ns ? ptx::mbar_try_wait_suspend(bar, parity, suspend_ns) : ptx::mbar_try_wait(bar, parity))
-            return true;
+        if (poll()) return true;
         if (abort && *abort) return false;
         if (ptx::global_timer_ns() - t0 > timeout_ns) return false;
     }
@@ -336,11 +340,15 @@ __device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, con
 
 // After a failed wait at box k: stop the producer, then wait (bounded) for
 // every load it already started so that no copy lands in shared memory after
-// the CTA exits.  Called by one thread, after bulk_wait_all().
+// the CTA exits.  Called by one thread, after bulk_wait_all().  The drain has
+// its own budget of at least one second, so that a very short wait limit
+// still leaves time for copies that are merely slow.
+constexpr uint64_t kMinDrainNs = 1000000000ull;
+
 __device__ void drain_after_failure(const PipeArgs& a, const Ring& r, uint32_t k)
 {
     raise_abort(a, r, tile_of(a, k), kWhereConsumerWait);
-    const uint64_t deadline = ptx::global_timer_ns() + a.timeout_ns;
+    const uint64_t deadline = ptx::global_timer_ns() + (a.timeout_ns > kMinDrainNs ? a.timeout_ns : kMinDrainNs);
     while (!*reinterpret_cast<volatile uint32_t*>(&r.ctl->producer_done) && ptx::global_timer_ns() < deadline) {
     }
     const uint32_t issued = *reinterpret_cast<volatile uint32_t*>(&r.ctl->issued);

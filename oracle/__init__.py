@@ -60,7 +60,9 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
+        # ORACLE_LIB lets the mutation tests run the pins against a deliberately
+        # broken build of this same source; it is never set otherwise.
+        lib = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
         P = ctypes.POINTER(_View)
         u8p = ctypes.c_void_p
         lib.oracle_swizzle.argtypes = [ctypes.c_uint64, ctypes.c_int32]

@@ -558,3 +558,32 @@ def test_tensor_larger_than_4gib(atb):
     sample[-1] = (cols - 64, rows - 128)  # the box with the largest offsets
     assert_bytes_equal(oracle.tile_load(v, dst_h, sample), oracle.tile_load(v, src_h, sample), "4.5 GiB sampled",
                        image_bytes=oracle.box_bytes(v))
+
+
+
+def test_two_million_small_boxes(atb):
+    # many boxes in one call: 2^21 listed 16-byte boxes (list indices past 2^20)
+    n = 1 << 21
+    dims = (4096, 1024)
+    v = oracle.View(1, dims, (1, 4096), (16, 1))
+    src_h = datagen.random_bytes(4096 * 1024, 777)
+    g = datagen.rng(778)
+    coords_h = np.stack([g.integers(-1, 257, n) * 16, g.integers(-1, 1025, n)], 1).astype(np.int32)
+    src = dev_bytes(src_h)
+    coords = dev_bytes(coords_h.view(np.uint8))
+    ms = atb.encode_tiled("u8", src, dims, v.strides, v.box)
+    packed = dev_empty(n * 16, fill=0xEE)
+    atb.tile_load(ms, coords, n, packed)
+    device_ok(atb)
+    assert_bytes_equal(host(packed), oracle.tile_load(v, src_h, coords_h), "2M boxes", image_bytes=16)
+
+
+def test_sixteen_stages_and_single_cta(atb):
+    w = datagen.C2
+    src_h = datagen.storage(w, seed=16)
+    src, dst = dev_bytes(src_h), dev_empty(w.storage_bytes, fill=0)
+    m16 = atb.encode_tiled("f16", src, (1792, 8448), (2, 3584), (64, 32))  # 4 KiB boxes
+    d16 = atb.encode_tiled("f16", dst, (1792, 8448), (2, 3584), (64, 32))
+    atb.tile_roundtrip(m16, d16, stages=16, ctas=1, store_groups=8)
+    device_ok(atb)
+    assert_bytes_equal(host(dst), src_h, "16 stages, one CTA")
