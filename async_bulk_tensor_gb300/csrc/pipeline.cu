@@ -777,7 +777,7 @@ atb_status noalloc_scratch_address(const DeviceInfo& dev, void** out)
 // Per-device streams and events that overlap the host-to-device copies, the
 // round trips and the device-to-host copies of atb_tile_roundtrip_host.
 constexpr uint32_t kMaxHostSlabs = 64;
-constexpr uint32_t kDefaultHostSlabs = 8;
+constexpr uint32_t kDefaultHostSlabs = 12;
 
 struct HostPipe {
     bool ready;

@@ -306,6 +306,12 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
             s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, stages=stages),
                               steps, 5)
             out[key] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
+        for promo in ("128B", "256B"):  # L2 promotion of the source map, default pipeline
+            mp = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle, promo)
+            s = time_launches(torch, stream, lambda: atb.tile_roundtrip(mp, md, stream=stream), steps, 5)
+            out[f"{box}_s3_l2promotion{promo}"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
+        s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, pdl=False), steps, 5)
+        out[f"{box}_s3_without_pdl"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
     return out
 
 
@@ -403,6 +409,26 @@ def workload_lines(torch, atb, datagen, device, stream, args):
         out[w.name + f"_load_prefetch{pf}"] = line(inb + n * bb, n, warm, cold)
     warm, cold = timed(lambda: atb.tile_store(mf, coords, n, packed, stream=stream), 500, 30)
     out[w.name + "_store"] = line(n * bb + inb, n, warm, cold)
+    del src, packed, fresh
+
+    # the fp32 update between load and store: 16384 x 8192 fp32 (512 MiB), box 32x128, 128B swizzle
+    rows, cols = 8192, 16384
+    a32 = torch.empty(rows * cols * 4, dtype=torch.uint8, device=device)
+    a32.view(torch.float32).normal_()
+    b32 = torch.empty_like(a32)
+    ma = atb.encode_tiled("f32", a32, (cols, rows), (4, cols * 4), (32, 128), "128B")
+    mb = atb.encode_tiled("f32", b32, (cols, rows), (4, cols * 4), (32, 128), "128B")
+    warm, cold = timed(lambda: atb.tile_roundtrip_add_f32(ma, mb, 1.0, stream=stream), 300, 10)
+    out["f32_16384x8192_add1_roundtrip"] = line(2 * rows * cols * 4, atb.grid_tiles(ma), warm, cold)
+    warm, cold = timed(lambda: atb.tile_roundtrip(ma, mb, stream=stream), 300, 10)
+    out["f32_16384x8192_plain_roundtrip"] = line(2 * rows * cols * 4, atb.grid_tiles(ma), warm, cold)
+    # traversal step 2 along rows: every other row of each 64-row box, gathered to packed images
+    ms2 = atb.encode_tiled("f32", a32, (cols, rows), (4, cols * 4), (32, 64), "128B", elem_strides=(1, 2))
+    bb2 = atb.box_bytes(ms2)
+    n2 = atb.grid_tiles(ms2)
+    packed2 = torch.empty(n2 * bb2, dtype=torch.uint8, device=device)
+    warm, cold = timed(lambda: atb.tile_load(ms2, None, 0, packed2, stream=stream), 300, 10)
+    out["f32_16384x8192_step2_rows_gather"] = line(2 * n2 * bb2, n2, warm, cold)
     atb.check_device(stream)
     return out
 
@@ -440,7 +466,7 @@ def end_to_end(torch, atb, w, device, stream, src_h, nbytes, bytes_per_step, arg
     units, max_s = aggregate(dist, seconds, float(bytes_per_step) * steps, device)
     return {"value": round(units / max_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": nbytes, "steps": steps, "ms_per_step": round(max_s / steps * 1e3, 3),
-            "slabs": args.slabs or 8, "call": "atb_tile_roundtrip_host", "verified_sample": ok}
+            "slabs": args.slabs or 12, "call": "atb_tile_roundtrip_host", "verified_sample": ok}
 
 
 def cpu_baseline(w, src_h, repeats: int = 4):

@@ -312,7 +312,7 @@ atb_status atb_tile_roundtrip(const atb_tensor_map* src, const atb_tensor_map* d
  *   h_dst     host memory laid out as `dst` describes its device buffer;
  *             bytes between rows (padding) may be overwritten with the
  *             device buffer's contents
- *   slabs     0 = 8; clamped to 1..64 and to the number of box rows.  When
+ *   slabs     0 = 12; clamped to 1..64 and to the number of box rows.  When
  *             the outermost stride does not step over the whole inner span
  *             (a permuted view), the call uses one slab.
  * Not for concurrent use from several host threads on one device (the
