@@ -336,17 +336,18 @@ atb_status atb_device_status(atb_stream_t stream, atb_device_report* report)
 {
     clear_error();
     DeviceStatus* st = nullptr;
-    atb_status s = device_status_block(&st);
-    if (s != ATB_OK) return s;
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_error(e, "cudaStreamSynchronize");
+    atb_status rc = device_status_block(&st);
+    if (rc != ATB_OK) return rc;
+    // Read and clear the record in stream order, after everything already
+    // queued on `stream`; work on other streams is not waited for.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DeviceStatus host{};
-    e = cudaMemcpy(&host, st, sizeof host, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_error(e, "cudaMemcpy(status block)");
-    e = cudaMemset(st, 0, sizeof host);
-    if (e != cudaSuccess) return cuda_error(e, "cudaMemset(status block)");
-    e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_error(e, "cudaDeviceSynchronize");
+    cudaError_t e = cudaMemcpyAsync(&host, st, sizeof host, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_error(e, "cudaMemcpyAsync(status block)");
+    e = cudaMemsetAsync(st, 0, sizeof host, s);
+    if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync(status block)");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "cudaStreamSynchronize");
     if (report) memcpy(report, &host, sizeof host);
     return static_cast<atb_status>(host.code);
 }

@@ -351,8 +351,11 @@ atb_status atb_tile_roundtrip_add_f32(const atb_tensor_map* src, const atb_tenso
 atb_status atb_init_device(void);
 
 /*
- * Synchronise `stream`, copy the current device's status block into *report
- * (may be NULL) and reset it.  Returns the recorded code (ATB_OK if none).
+ * After the work already queued on `stream`, copy the current device's
+ * status block into *report (may be NULL) and reset it, then wait for that.
+ * Returns the recorded code (ATB_OK if none).  The block is shared by every
+ * stream of the device: kernels still running on other streams may record
+ * errors after the read; synchronise them first to include them.
  */
 atb_status atb_device_status(atb_stream_t stream, atb_device_report* report);
 
