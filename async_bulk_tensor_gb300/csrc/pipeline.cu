@@ -200,39 +200,93 @@ __device__ __forceinline__ int store_kind(const PipeArgs& a, const int32_t (&c)[
 // boundary in both spaces (the origin's x is 16-byte aligned, strides are
 // multiples of 16), so a chunk that lies wholly inside the tensor moves as one
 // vector; only a chunk cut by the end of a row moves element by element.
+//
+// Threads are laid out as `group` rows of `cpr` chunks (or, for rows wider
+// than the thread count, one row at a time).  The box is walked plane by plane
+// (dimensions 2..R-1, decomposed once per plane) and, inside a plane, row by
+// row along dimension 1 with additions only: a single warp runs this loop
+// alone, so short dependency chains matter more than instruction counts.
 template <int R>
-__device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], const uint8_t* stage, uint32_t tid,
+__device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage, uint32_t tid,
                                 uint32_t nthreads)
 {
     const uint32_t row_bytes = a.box[0] * a.esize;  // the innermost step is always 1
-    const uint32_t chunks_per_row = row_bytes / 16;
+    const uint32_t cpr = row_bytes / 16;             // 16-byte chunks per row
     const uint32_t rows = a.box_bytes / row_bytes;
+    const uint32_t group = cpr < nthreads ? nthreads / cpr : 1;  // rows in flight per pass
+    const uint32_t jstep = cpr < nthreads ? cpr : nthreads;
+    const uint32_t first_row = tid / cpr;
+    if (first_row >= group) return;  // threads beyond group * cpr have no chunk
+    const uint32_t j0 = tid - first_row * cpr;
     const uint32_t q = 16 / a.esize;  // elements per chunk
     const uint32_t line_mask = (1u << a.swizzle_bits) - 1u;
     const int64_t dims0 = static_cast<int64_t>(a.dst_dims[0]);
-    for (uint32_t i = tid; i < rows * chunks_per_row; i += nthreads) {
-        const uint32_t row = i / chunks_per_row, j = i - row * chunks_per_row;
-        uint32_t rest = row;
+    const uint32_t rows1 = R > 1 ? a.visits[1] : 1;  // rows per plane
+    const uint32_t planes = rows / rows1;
+    const int64_t dims1 = R > 1 ? static_cast<int64_t>(a.dst_dims[1]) : 1;
+    const int64_t gstep1 = R > 1 ? static_cast<int64_t>(group) * a.step[1] : 0;
+    const uint64_t stride1 = R > 1 ? a.dst_strides[1] : 0;
+
+    // One 16-byte column per thread (the usual case: a row fits in the thread
+    // group): the column's x offset, bounds and swizzle-free part are fixed,
+    // so each row costs a bounds check, two address additions and the copy.
+    const bool one_column = cpr <= nthreads;
+    const int64_t xc = static_cast<int64_t>(c[0]) + static_cast<int64_t>(j0) * q;
+    if (one_column && (xc < 0 || xc >= dims0)) return;  // this column lies outside every row
+    const bool xc_whole = xc + q <= dims0;
+
+    for (uint32_t plane = 0; plane < planes; ++plane) {
+        uint32_t rest = plane;
         bool inside = true;
-        uint64_t addr = 0;
+        uint64_t plane_addr = 0;
 #pragma unroll
-        for (int d = 1; d < R; ++d) {
+        for (int d = 2; d < R; ++d) {
             const uint32_t k = rest % a.visits[d];
             rest /= a.visits[d];
             const int64_t g = static_cast<int64_t>(c[d]) + static_cast<int64_t>(k) * a.step[d];
             if (g < 0 || g >= static_cast<int64_t>(a.dst_dims[d])) inside = false;
-            else addr += static_cast<uint64_t>(g) * a.dst_strides[d];
+            else plane_addr += static_cast<uint64_t>(g) * a.dst_strides[d];
         }
-        const int64_t x0 = static_cast<int64_t>(c[0]) + static_cast<int64_t>(j) * q;  // first element of the chunk
-        if (!inside || x0 < 0 || x0 >= dims0) continue;
-        const uint32_t o = row * row_bytes + 16 * j;
-        const uint8_t* src = stage + (o ^ (((o >> 7) & line_mask) << 4));
-        uint8_t* dst = a.dst_base + addr + static_cast<uint64_t>(x0) * a.esize;
-        if (x0 + q <= dims0) {
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        if (!inside) continue;
+        int64_t g1 = R > 1 ? static_cast<int64_t>(c[1]) + static_cast<int64_t>(first_row) * a.step[1] : 0;
+        uint32_t o_row = (plane * rows1 + first_row) * row_bytes;
+        if (one_column) {
+            uint8_t* col = a.dst_base + plane_addr + static_cast<uint64_t>(xc) * a.esize;
+            const uint32_t row_step = group * row_bytes;
+#pragma unroll 4
+            for (uint32_t k1 = first_row; k1 < rows1; k1 += group, g1 += gstep1, o_row += row_step) {
+                if (g1 < 0 || g1 >= dims1) continue;
+                const uint32_t o = o_row + 16 * j0;
+                const uint32_t src = stage + (o ^ (((o >> 7) & line_mask) << 4));
+                uint8_t* dst = col + static_cast<uint64_t>(g1) * stride1;
+                if (xc_whole) {
+                    *reinterpret_cast<uint4*>(dst) = ptx::ld_shared_v4_u32(src);
+                } else {
+                    for (uint32_t b = 0; b < static_cast<uint32_t>(dims0 - xc) * a.esize; ++b)
+                        dst[b] = ptx::ld_shared_u8(src + b);
+                }
+            }
             continue;
         }
-        for (uint32_t b = 0; b < static_cast<uint32_t>(dims0 - x0) * a.esize; ++b) dst[b] = src[b];
+        for (uint32_t k1 = first_row; k1 < rows1; k1 += group, g1 += gstep1, o_row += group * row_bytes) {
+            if (g1 < 0 || g1 >= dims1) continue;
+            const uint64_t addr = plane_addr + static_cast<uint64_t>(g1) * stride1;
+            for (uint32_t j = j0; j < cpr; j += jstep) {
+                const int64_t x0 = static_cast<int64_t>(c[0]) + static_cast<int64_t>(j) * q;
+                if (x0 < 0 || x0 >= dims0) continue;
+                const uint32_t o = o_row + 16 * j;
+                // explicit shared-space loads: a generic load could alias the
+                // global stores before it and would wait for them to finish
+                const uint32_t src = stage + (o ^ (((o >> 7) & line_mask) << 4));
+                uint8_t* dst = a.dst_base + addr + static_cast<uint64_t>(x0) * a.esize;
+                if (x0 + q <= dims0) {
+                    *reinterpret_cast<uint4*>(dst) = ptx::ld_shared_v4_u32(src);
+                } else {
+                    for (uint32_t b = 0; b < static_cast<uint32_t>(dims0 - x0) * a.esize; ++b)
+                        dst[b] = ptx::ld_shared_u8(src + b);
+                }
+            }
+        }
     }
 }
 
@@ -355,6 +409,40 @@ __device__ void drain_after_failure(const PipeArgs& a, const Ring& r, uint32_t k
     for (uint32_t j = k; j < issued; ++j) wait_until(r.full(j % r.stages), (j / r.stages) & 1, deadline);
 }
 
+// Store groups that may still be reading their stages, oldest first: the
+// stage index (4 bits, stages <= 16) and the consumer's box counter modulo 256
+// (8 bits) of each, at most 8 in flight.  Only boxes the engine stores have a
+// group; a box written by threads, or dropped, frees its stage as soon as its
+// readers are done.  After every box k, each group started at least `lag`
+// boxes earlier is retired, so a stage is always free again by the time the
+// producer comes back to it (lag < stages).
+struct PendingStores {
+    uint64_t stages = 0;
+    uint64_t boxes = 0;
+    uint32_t count = 0;
+
+    __device__ __forceinline__ void push(uint32_t stage, uint32_t box)
+    {
+        stages |= static_cast<uint64_t>(stage) << (4 * count);
+        boxes |= static_cast<uint64_t>(box & 255u) << (8 * count);
+        ++count;
+    }
+
+    __device__ __forceinline__ void retire(const Ring& r, uint32_t k, uint32_t lag)
+    {
+        uint32_t keep = 0;  // groups younger than `lag` boxes may stay in flight
+        for (uint32_t i = 0; i < count; ++i)
+            if (((k - static_cast<uint32_t>((boxes >> (8 * i)) & 255u)) & 255u) < lag) ++keep;
+        if (keep == count) return;
+        ptx::bulk_wait_read_le(keep);
+        for (; count > keep; --count) {
+            ptx::mbar_arrive(r.empty(static_cast<uint32_t>(stages & 15u)));
+            stages >>= 4;
+            boxes >>= 8;
+        }
+    }
+};
+
 template <int MODE, int R>
 __global__ void __launch_bounds__(kPipelineThreads, 1)
     tile_pipeline_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
@@ -388,7 +476,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
     const uint64_t store_policy = !store_hint ? 0
                                   : (a.l2_hints & ATB_HINT_STORE_EVICT_FIRST) ? ptx::policy_evict_first()
                                                                                : ptx::policy_evict_last();
-    uint32_t next_release = 0;  // boxes [next_release, k) still have a group reading their stage
+    PendingStores pending;  // lane 0's store groups still reading their stages
     uint32_t k = 0;
     bool failed = false;
     for (; k < count; ++k) {
@@ -407,7 +495,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
 
         if (kind == kStorePlain) {
             // boxes the engine may not store: the warp writes them itself
-            plain_store_box<R>(a, c, r.stage_ptr(s), lane, 32);
+            plain_store_box<R>(a, c, r.stage(s), lane, 32);
             __syncwarp();
         }
         if (lane == 0) {
@@ -419,12 +507,12 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
                     ptx::tma_store_hint<R>(&dst_map, c, r.stage(s), store_policy);
                 else
                     ptx::tma_store<R>(&dst_map, c, r.stage(s));
+                ptx::bulk_commit();
+                pending.push(s, k);
+            } else {
+                ptx::mbar_arrive(r.empty(s));  // written by the warp, or nothing to write
             }
-            // One group per box (an empty one when the engine stores nothing),
-            // so that the groups still reading map to boxes [k - lag, k].
-            ptx::bulk_commit();
-            ptx::bulk_wait_read_le(a.store_lag);
-            for (; next_release + a.store_lag <= k; ++next_release) ptx::mbar_arrive(r.empty(next_release % S));
+            pending.retire(r, k, a.store_lag);
         }
     }
 
@@ -466,7 +554,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
 
     const uint32_t ct = threadIdx.x - 32;  // consumer thread 0 .. kConsumerThreads-1
     const uint32_t chunks = a.box_bytes / 16;
-    uint32_t next_release = 0;
+    PendingStores pending;  // consumer thread 0's store groups still reading their stages
     uint32_t k = 0;
     bool failed = false;
     for (; k < count; ++k) {
@@ -498,14 +586,18 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
         }
         ptx::named_barrier_sync(1, kConsumerThreads);
         if (kind == kStorePlain) {
-            plain_store_box<R>(a, c, r.stage_ptr(s), ct, kConsumerThreads);
+            plain_store_box<R>(a, c, r.stage(s), ct, kConsumerThreads);
             ptx::named_barrier_sync(1, kConsumerThreads);  // every reader is done with the stage
         }
         if (ct == 0) {
-            if (kind == kStoreTensor) ptx::tma_store<R>(&dst_map, c, r.stage(s));
-            ptx::bulk_commit();  // one group per box, empty when the engine stores nothing
-            ptx::bulk_wait_read_le(a.store_lag);
-            for (; next_release + a.store_lag <= k; ++next_release) ptx::mbar_arrive(r.empty(next_release % S));
+            if (kind == kStoreTensor) {
+                ptx::tma_store<R>(&dst_map, c, r.stage(s));
+                ptx::bulk_commit();
+                pending.push(s, k);
+            } else {
+                ptx::mbar_arrive(r.empty(s));  // written by the threads, or nothing to write
+            }
+            pending.retire(r, k, a.store_lag);
         }
     }
 

@@ -109,6 +109,23 @@ __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads,
     return out != 0;
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4_u32(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint8_t ld_shared_u8(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return static_cast<uint8_t>(v);
+}
+
 __device__ __forceinline__ void ld_shared_v4_f32(uint32_t addr, float (&v)[4])
 {
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
