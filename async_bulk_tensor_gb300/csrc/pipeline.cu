@@ -11,8 +11,9 @@
 //                   image), commits it as a bulk async group and, once
 //                   wait_group.read shows the group has finished reading the
 //                   stage, arrives on the stage's "empty" mbarrier.  Boxes a
-//                   tensor store may not start (a negative origin) are written
-//                   by the whole warp with plain clipped stores.
+//                   tensor store may not write (a negative origin, or a ragged
+//                   row end) are written by the whole warp with plain clipped
+//                   stores, and their stages are freed at once.
 //
 // Sources: "lesson 04: TMA - the async bulk copy engine" ("What the issuing
 // thread actually does", "Load completion - the mbarrier and the byte budget",
@@ -275,8 +276,6 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32
                 const int64_t x0 = static_cast<int64_t>(c[0]) + static_cast<int64_t>(j) * q;
                 if (x0 < 0 || x0 >= dims0) continue;
                 const uint32_t o = o_row + 16 * j;
-                // explicit shared-space loads: a generic load could alias the
-                // global stores before it and would wait for them to finish
                 const uint32_t src = stage + (o ^ (((o >> 7) & line_mask) << 4));
                 uint8_t* dst = a.dst_base + addr + static_cast<uint64_t>(x0) * a.esize;
                 if (x0 + q <= dims0) {
@@ -302,7 +301,6 @@ struct Ring {
     Control* ctl;
 
     __device__ uint32_t stage(uint32_t s) const { return base + s * stage_bytes; }
-    __device__ uint8_t* stage_ptr(uint32_t s) const { return base_ptr + s * stage_bytes; }
     __device__ uint32_t full(uint32_t s) const { return full0 + 8 * s; }
     __device__ uint32_t empty(uint32_t s) const { return empty0 + 8 * s; }
     __device__ volatile uint32_t* abort_flag() const { return &ctl->abort; }
