@@ -159,6 +159,64 @@ __device__ __forceinline__ void tile_origin(const PipeArgs& a, uint32_t t, int32
     }
 }
 
+// Walks one CTA's boxes in order with additions only: the ring stage and the
+// parity of its current use, the box's index in the list or grid and, for the
+// grid, its tile coordinates.  The step between consecutive boxes (gridDim.x,
+// or 1 for contiguous runs) is kept in the grid's mixed radix and added digit
+// by digit, with at most one carry per dimension.
+template <int R>
+struct BoxCursor {
+    uint32_t stage = 0;
+    uint32_t parity = 0;
+    uint32_t t = 0;   // index in the list or grid
+    uint32_t g[R];    // tile coordinates (grid)
+    uint32_t dg[R];   // the step, digit by digit
+
+    __device__ __forceinline__ void init(const PipeArgs& a)
+    {
+        t = tile_of(a, 0);
+        uint32_t rest = t, rstep = a.contiguous ? 1u : gridDim.x;
+#pragma unroll
+        for (int d = 0; d < R - 1; ++d) {
+            g[d] = rest % a.grid[d];
+            rest /= a.grid[d];
+            dg[d] = rstep % a.grid[d];
+            rstep /= a.grid[d];
+        }
+        g[R - 1] = rest;
+        dg[R - 1] = rstep;
+    }
+
+    __device__ __forceinline__ void origin(const PipeArgs& a, int32_t (&c)[R]) const
+    {
+        if (a.coords) {
+            const int32_t* p = a.coords + static_cast<size_t>(t) * R;
+#pragma unroll
+            for (int d = 0; d < R; ++d) c[d] = __ldg(p + d);
+        } else {
+#pragma unroll
+            for (int d = 0; d < R; ++d) c[d] = static_cast<int32_t>(g[d] * a.box[d]);
+        }
+    }
+
+    __device__ __forceinline__ void advance(const PipeArgs& a, uint32_t stages)
+    {
+        if (++stage == stages) {
+            stage = 0;
+            parity ^= 1u;
+        }
+        t += a.contiguous ? 1u : gridDim.x;
+        uint32_t carry = 0;
+#pragma unroll
+        for (int d = 0; d < R - 1; ++d) {
+            g[d] += dg[d] + carry;
+            carry = g[d] >= a.grid[d] ? 1u : 0u;
+            if (carry) g[d] -= a.grid[d];
+        }
+        g[R - 1] += dg[R - 1] + carry;
+    }
+};
+
 // A listed origin the engine must not be given: beyond +-2^30, or not on a
 // 16-byte boundary along the contiguous dimension.
 template <int R>
@@ -358,20 +416,23 @@ __device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, con
             if (!origin_error<R>(a, c)) ptx::tma_prefetch_l2<R>(&src_map, c);
         }
     }
-    for (uint32_t k = 0; k < count; ++k) {
-        const uint32_t s = k % S, use = k / S;
+    BoxCursor<R> cur;
+    cur.init(a);
+    for (uint32_t k = 0; k < count; ++k, cur.advance(a, S)) {
+        const uint32_t s = cur.stage;
         if (MODE != kStore && a.prefetch && k + a.prefetch < count) {
             int32_t c[R];
             tile_origin<R>(a, tile_of(a, k + a.prefetch), c);
             if (!origin_error<R>(a, c)) ptx::tma_prefetch_l2<R>(&src_map, c);
         }
-        if (k >= S && !wait_bounded(r.empty(s), (use - 1) & 1, a.timeout_ns, r.abort_flag(), a.suspend_ns)) {
-            raise_abort(a, r, tile_of(a, k), kWhereProducerWait);
+        // the stage's previous use completed the empty phase of the other parity
+        if (k >= S && !wait_bounded(r.empty(s), cur.parity ^ 1u, a.timeout_ns, r.abort_flag(), a.suspend_ns)) {
+            raise_abort(a, r, cur.t, kWhereProducerWait);
             break;
         }
-        const uint32_t t = tile_of(a, k);
+        const uint32_t t = cur.t;
         int32_t c[R];
-        tile_origin<R>(a, t, c);
+        cur.origin(a, c);
         const int32_t bad = origin_error<R>(a, c);
         if (bad) {
             record_error(a.status, bad, static_cast<int32_t>(t), kWhereProducerIssue);
@@ -475,18 +536,20 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
                                   : (a.l2_hints & ATB_HINT_STORE_EVICT_FIRST) ? ptx::policy_evict_first()
                                                                                : ptx::policy_evict_last();
     PendingStores pending;  // lane 0's store groups still reading their stages
+    BoxCursor<R> cur;
+    cur.init(a);
     uint32_t k = 0;
     bool failed = false;
-    for (; k < count; ++k) {
-        const uint32_t s = k % S, parity = (k / S) & 1;
-        const bool ok = wait_bounded(r.full(s), parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
+    for (; k < count; ++k, cur.advance(a, S)) {
+        const uint32_t s = cur.stage;
+        const bool ok = wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
         if (!__all_sync(0xffffffffu, ok)) {
             failed = true;
             break;
         }
-        const uint32_t t = tile_of(a, k);
+        const uint32_t t = cur.t;
         int32_t c[R];
-        tile_origin<R>(a, t, c);
+        cur.origin(a, c);
         const bool skip = origin_error<R>(a, c) != 0;
         // kLoad: kStoreTensor means "drain the image to the packed buffer"
         const int kind = skip ? kStoreNothing : (MODE == kLoad ? kStoreTensor : store_kind<R>(a, c));
@@ -553,11 +616,13 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
     const uint32_t ct = threadIdx.x - 32;  // consumer thread 0 .. kConsumerThreads-1
     const uint32_t chunks = a.box_bytes / 16;
     PendingStores pending;  // consumer thread 0's store groups still reading their stages
+    BoxCursor<R> cur;
+    cur.init(a);
     uint32_t k = 0;
     bool failed = false;
-    for (; k < count; ++k) {
-        const uint32_t s = k % S, parity = (k / S) & 1;
-        const bool ok = wait_bounded(r.full(s), parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
+    for (; k < count; ++k, cur.advance(a, S)) {
+        const uint32_t s = cur.stage;
+        const bool ok = wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
         if (!__all_sync(0xffffffffu, ok)) {
             failed = true;
         }
@@ -566,9 +631,8 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
             failed = true;
             break;
         }
-        const uint32_t t = tile_of(a, k);
         int32_t c[R];
-        tile_origin<R>(a, t, c);
+        cur.origin(a, c);
         const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
         if (kind != kStoreNothing) {
             // generic-proxy update of the landed box; element order is irrelevant

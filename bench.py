@@ -40,6 +40,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 NOMINAL_HBM_GBS = 8000.0
+REF_BOX_BUDGET = 250_000  # reference arm: boxes over the whole run (~0.2 ms each)
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "tile_pipeline_roundtrip_f16_16384.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "async_bulk_tensor_gb300", "csrc", f) for f in ("pipeline.cu", "ptx.cuh")]
@@ -504,7 +505,9 @@ def run_reference(args):
     w = datagen.C5A if args.box == "64x256" else datagen.C5B
     v = oracle.View(w.esize, w.dims, w.strides, w.box, w.swizzle)
     coords = oracle.grid_coords(v)
-    sample_tiles = args.ref_tiles
+    # Boxes per step: as given, else sized so that warm-up plus timed steps
+    # stay under about a minute of single-core oracle work.
+    sample_tiles = args.ref_tiles or max(8, min(1024, REF_BOX_BUDGET // (args.steps + args.warmup)))
     sample = coords[:sample_tiles]
     src_h = datagen.storage(w)
     dst = np.zeros_like(src_h)
@@ -541,7 +544,8 @@ def main(argv=None):
     p.add_argument("--poll-suspend-ns", type=int, default=0, help="mbarrier poll suspend hint (0 = default)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--slabs", type=int, default=0, help="host round trip slabs (0 = library default)")
-    p.add_argument("--ref-tiles", type=int, default=1024, help="boxes per reference-arm step")
+    p.add_argument("--ref-tiles", type=int, default=0,
+                   help="boxes per reference-arm step (0 = sized from --steps/--warmup)")
     p.add_argument("--no-extras", action="store_true", help="skip the stage sweep and ablations")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
