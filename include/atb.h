@@ -30,6 +30,11 @@
  *     default stream).  Host-detectable errors return before anything is
  *     launched; atb_last_error() then holds a sentence naming the rule, the
  *     dimension and the value.
+ *   - atb_tile_load, atb_tile_store, atb_tile_roundtrip and
+ *     atb_tile_roundtrip_add_f32 can be captured into CUDA graphs (stream
+ *     capture) once atb_init_device() and one call of the same kind have run
+ *     outside the capture on that device; a replay moves whatever the
+ *     captured maps' buffers hold at replay time.
  *   - Pipeline kernels are launched with programmatic dependent launch: a
  *     launch may be scheduled while the previous kernel on the stream drains,
  *     sets up its shared memory, and waits for that kernel to complete (with

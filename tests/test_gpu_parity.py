@@ -587,3 +587,45 @@ def test_sixteen_stages_and_single_cta(atb):
     atb.tile_roundtrip(m16, d16, stages=16, ctas=1, store_groups=8)
     device_ok(atb)
     assert_bytes_equal(host(dst), src_h, "16 stages, one CTA")
+
+
+# --------------------------------------------------------------------------
+# CUDA graphs: the calls capture into a graph and replay exactly
+# --------------------------------------------------------------------------
+def test_cuda_graph_capture_and_replay(atb):
+    torch = torch_cuda()
+    w = datagen.C3
+    v = oracle_view(w)
+    src_h = datagen.storage(w)
+    src = dev_bytes(src_h)
+    ms = encode(atb, w, src)
+    n = atb.grid_tiles(ms)
+    bb = atb.box_bytes(ms)
+    packed = dev_empty(n * bb, fill=0)
+    out = dev_empty(w.storage_bytes, fill=0)
+    md = encode(atb, w, out)
+    atb.init_device()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # first calls outside the capture (per-kernel set-up)
+        atb.tile_load(ms, None, 0, packed)
+        atb.tile_store(md, None, 0, packed)
+        atb.tile_roundtrip(ms, md)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        atb.tile_load(ms, None, 0, packed)   # grid gather into packed images
+        atb.tile_store(md, None, 0, packed)  # and back into the second tensor
+        atb.tile_roundtrip(ms, md)           # then a direct round trip over it
+    for seed in (31, 32):
+        new_h = datagen.storage(w, seed=seed)
+        src.copy_(torch.from_numpy(new_h))
+        out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        device_ok(atb)
+        assert_bytes_equal(host(packed), oracle.tile_load(v, new_h, oracle.grid_coords(v)), f"graph gather {seed}",
+                           image_bytes=bb)
+        want = np.zeros_like(new_h)
+        oracle.roundtrip(v, new_h, v, want, oracle.grid_coords(v))
+        assert_bytes_equal(host(out), want, f"graph round trip {seed}")
