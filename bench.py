@@ -202,6 +202,21 @@ def time_launches(torch, stream, fn, steps: int, warmup: int, dist=None, device=
     return start.elapsed_time(end) / 1e3
 
 
+def single_steps(torch, stream, fn, n: int):
+    """Milliseconds of n steps, each bracketed by its own pair of events."""
+    out = []
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+    return out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -246,6 +261,7 @@ def run_gpu(args):
     with ClockSampler(gpu_id) as clocks:
         seconds = time_launches(torch, stream, step, args.steps, args.warmup, dist, device)
     atb.check_device(stream)
+    per_step = single_steps(torch, stream, step, 20)
     units, max_seconds = aggregate(dist, seconds, float(bytes_per_step) * args.steps, device)
     value = units / max_seconds / 1e9
     ms_per_step = max_seconds / args.steps * 1e3
@@ -266,6 +282,11 @@ def run_gpu(args):
         "l2": "inputs larger than L2 (512 MiB read + 512 MiB written per step); no flush",
     }
     result["tiles_per_s"] = round(tiles * args.steps * world / max_seconds, 1)
+    result["single_steps"] = {"n": len(per_step), "ms_median": round(statistics.median(per_step), 5),
+                              "ms_best": round(min(per_step), 5),
+                              "GBps_median": round(bytes_per_step / statistics.median(per_step) / 1e6, 1),
+                              "GBps_best": round(bytes_per_step / min(per_step) / 1e6, 1),
+                              "note": "each step timed alone between events (launch gap included)"}
     peak, peak_kind = hbm_peak()
     traffic, traffic_note = committed_traffic()
     result["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

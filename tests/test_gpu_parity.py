@@ -616,6 +616,26 @@ def test_cuda_graph_capture_and_replay(atb):
         atb.tile_load(ms, None, 0, packed)   # grid gather into packed images
         atb.tile_store(md, None, 0, packed)  # and back into the second tensor
         atb.tile_roundtrip(ms, md)           # then a direct round trip over it
+    # the fp32 update, captured on its own: 256x256 fp32, sixteen 64x64 tiles, +1.0f
+    v32 = oracle.View(4, (256, 256), (4, 1024), (64, 64))
+    a32, b32 = dev_empty(256 * 1024), dev_empty(256 * 1024, fill=0)
+    m_a = atb.encode_tiled("f32", a32, v32.dims, v32.strides, v32.box)
+    m_b = atb.encode_tiled("f32", b32, v32.dims, v32.strides, v32.box)
+    with torch.cuda.stream(s):
+        atb.tile_roundtrip_add_f32(m_a, m_b, 1.0)
+    s.synchronize()
+    g32 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g32, stream=s):
+        atb.tile_roundtrip_add_f32(m_a, m_b, 1.0)
+    h32 = datagen.finite_f32_bytes(256 * 256, 33)
+    a32.copy_(torch.from_numpy(h32))
+    torch.cuda.synchronize()
+    g32.replay()
+    torch.cuda.synchronize()
+    want32 = np.zeros_like(h32)
+    oracle.roundtrip_add_f32(v32, h32, v32, want32, oracle.grid_coords(v32), 1.0)
+    assert_bytes_equal(host(b32), want32, "graph fp32 update")
+
     for seed in (31, 32):
         new_h = datagen.storage(w, seed=seed)
         src.copy_(torch.from_numpy(new_h))
