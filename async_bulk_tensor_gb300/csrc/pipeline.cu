@@ -582,17 +582,22 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
     if (failed) drain_after_failure(a, r, k);
 }
 
-// Round trip with an elementwise fp32 update in shared memory between the load
-// and the store ("Day 76: The Tensor Memory Accelerator (TMA)", "Exercise" and
-// "Solution": the threads change the tile in shared memory, every writer
-// publishes its writes across the proxy line with fence.proxy.async, the group
-// meets at a barrier, and one thread issues the tensor store).  Warp 0 lane 0
-// produces; warps 1..kTransformWarps update the stage, lane 0 of warp 1
-// issues the store.  Each element becomes x + addend in round-to-nearest fp32.
-template <int R>
+// The pipeline with four consumer warps: warp 0 lane 0 produces, warps 1..4
+// share each landed stage, and consumer thread 0 issues the tensor store.
+//   ADD   round trip with an elementwise fp32 update in shared memory between
+//         the load and the store ("Day 76: The Tensor Memory Accelerator
+//         (TMA)", "Exercise" and "Solution": the threads change the tile in
+//         shared memory, every writer publishes its writes across the proxy
+//         line with fence.proxy.async, the group meets at a barrier, and one
+//         thread issues the tensor store).  Each element becomes x + addend in
+//         round-to-nearest fp32.
+//   !ADD  a plain round trip or store whose boxes come from a list, where
+//         boxes that start before the tensor are common: 128 threads share
+//         the clipped stores of such boxes instead of one warp.
+template <int MODE, int R, bool ADD>
 __global__ void __launch_bounds__(kTransformThreads, 1)
-    tile_add_f32_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
-                        const PipeArgs a, float addend)
+    tile_wide_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
+                     const PipeArgs a, float addend)
 {
     extern __shared__ uint8_t smem_raw[];
     const Ring r = ring_layout(a, smem_raw);
@@ -600,7 +605,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) init_ring(r);
     if (threadIdx.x == 32) {
-        ptx::prefetch_tensor_map(&src_map);
+        if (MODE != kStore) ptx::prefetch_tensor_map(&src_map);
         ptx::prefetch_tensor_map(&dst_map);
     }
     ptx::launch_dependents();
@@ -609,7 +614,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
 
     const uint32_t count = my_tile_count(a);
     if (warp == 0) {
-        if (lane == 0) producer_loop<kRoundtrip, R>(a, src_map, r, count);
+        if (lane == 0) producer_loop<MODE, R>(a, src_map, r, count);
         return;
     }
 
@@ -634,7 +639,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
         int32_t c[R];
         cur.origin(a, c);
         const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
-        if (kind != kStoreNothing) {
+        if (ADD && kind != kStoreNothing) {
             // generic-proxy update of the landed box; element order is irrelevant
             const uint32_t base = r.stage(s);
             for (uint32_t j = ct; j < chunks; j += kConsumerThreads) {
@@ -653,6 +658,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
         }
         if (ct == 0) {
             if (kind == kStoreTensor) {
+                if (!ADD) ptx::fence_proxy_async_smem();  // (with ADD every writer fenced already)
                 ptx::tma_store<R>(&dst_map, c, r.stage(s));
                 ptx::bulk_commit();
                 pending.push(s, k);
@@ -683,7 +689,7 @@ __global__ void wait_timeout_selftest_kernel(DeviceStatus* st, uint64_t timeout_
 }
 
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PipeArgs);
-using AddKernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PipeArgs, float);
+using WideKernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PipeArgs, float);
 
 template <int MODE>
 KernelFn kernel_for_rank(uint32_t rank)
@@ -697,14 +703,15 @@ KernelFn kernel_for_rank(uint32_t rank)
     }
 }
 
-AddKernelFn add_kernel_for_rank(uint32_t rank)
+template <int MODE, bool ADD>
+WideKernelFn wide_kernel_for_rank(uint32_t rank)
 {
     switch (rank) {
-    case 1: return tile_add_f32_kernel<1>;
-    case 2: return tile_add_f32_kernel<2>;
-    case 3: return tile_add_f32_kernel<3>;
-    case 4: return tile_add_f32_kernel<4>;
-    default: return tile_add_f32_kernel<5>;
+    case 1: return tile_wide_kernel<MODE, 1, ADD>;
+    case 2: return tile_wide_kernel<MODE, 2, ADD>;
+    case 3: return tile_wide_kernel<MODE, 3, ADD>;
+    case 4: return tile_wide_kernel<MODE, 4, ADD>;
+    default: return tile_wide_kernel<MODE, 5, ADD>;
     }
 }
 
@@ -819,9 +826,15 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         if (st != ATB_OK) return st;
     }
 
-    const void* fn = MODE == kRoundtripAddF32 ? reinterpret_cast<const void*>(add_kernel_for_rank(rank))
-                                              : reinterpret_cast<const void*>(kernel_for_rank<MODE == kRoundtripAddF32 ? kRoundtrip : MODE>(rank));
-    const uint32_t threads = MODE == kRoundtripAddF32 ? kTransformThreads : kPipelineThreads;
+    // Listed boxes written to a tensor often start before it and need clipped
+    // thread stores: those launches (and the fp32 update) use four consumer warps.
+    constexpr int kBase = MODE == kRoundtripAddF32 ? kRoundtrip : MODE;
+    const bool wide = MODE == kRoundtripAddF32 || (MODE != kLoad && coords != nullptr);
+    WideKernelFn wide_fn = nullptr;
+    if (MODE == kRoundtripAddF32) wide_fn = wide_kernel_for_rank<kRoundtrip, true>(rank);
+    else if (wide) wide_fn = wide_kernel_for_rank<kBase == kLoad ? kRoundtrip : kBase, false>(rank);
+    const void* fn = wide ? reinterpret_cast<const void*>(wide_fn) : reinterpret_cast<const void*>(kernel_for_rank<kBase>(rank));
+    const uint32_t threads = wide ? kTransformThreads : kPipelineThreads;
     st = prepare_kernel(fn, dev);
     if (st != ATB_OK) return st;
 
@@ -889,11 +902,10 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     lc.attrs = attr;
     lc.numAttrs = cfg && cfg->no_pdl ? 0 : 1;
     cudaError_t e;
-    if (MODE == kRoundtripAddF32)
-        e = cudaLaunchKernelEx(&lc, add_kernel_for_rank(rank), src_map, dst_map, a, addend);
+    if (wide)
+        e = cudaLaunchKernelEx(&lc, wide_fn, src_map, dst_map, a, addend);
     else
-        e = cudaLaunchKernelEx(&lc, kernel_for_rank<MODE == kRoundtripAddF32 ? kRoundtrip : MODE>(rank), src_map,
-                               dst_map, a);
+        e = cudaLaunchKernelEx(&lc, kernel_for_rank<kBase>(rank), src_map, dst_map, a);
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     return ATB_OK;
 }
