@@ -15,6 +15,9 @@
 //                   row end) are written by the whole warp with plain clipped
 //                   stores, and their stages are freed at once.
 //
+// tile_wide_kernel runs the same ring with four consumer warps, for the fp32
+// update and for launches that write listed boxes into a tensor.
+//
 // Sources: "lesson 04: TMA - the async bulk copy engine" ("What the issuing
 // thread actually does", "Load completion - the mbarrier and the byte budget",
 // "Store completion - commit group and wait group", "Why this only pays off

@@ -264,11 +264,13 @@ atb_status atb_tile_load(const atb_tensor_map* src, const int32_t* d_coords, uin
  * stage with a 1-D bulk copy counted by the stage's mbarrier; the consumer
  * issues the tensor store, commits it and recycles the stage after
  * wait_group.read.  Elements outside the tensor are not written.  A box whose
- * origin is negative in any dimension is written by the consumer warp with
+ * origin is negative in any dimension is written by the consumer threads with
  * plain clipped stores instead (a tensor store may not start before the
  * tensor), and so is a box that crosses the end of a row whose byte length
  * (dims[0] x element size) is not a multiple of 16: the engine writes the
  * last 16-byte chunk of such a row whole, which would spill past the row.
+ * Calls with a coordinate list run four consumer warps, which share those
+ * clipped stores; calls over the tile grid run one.
  * Boxes that overlap with different contents land in an unspecified order.
  *
  *   dst       encoded map of the destination tensor
