@@ -231,48 +231,54 @@ def test_small_cases_all_ops(atb, case, launch):
     bb = atb.box_bytes(ms)
     n = coords_h.shape[0]
 
-    # gather, listed origins
-    packed = dev_empty(n * bb, fill=0xEE)
+    # gather, listed origins (guard bytes after the packed images must survive)
+    guard = 4096
+    packed = dev_empty(n * bb + guard, fill=0xEE)
     atb.tile_load(ms, coords, n, packed, **launch)
     device_ok(atb)
     want_packed = oracle.tile_load(v, src_h, coords_h)
-    assert_bytes_equal(host(packed), want_packed, f"{name} load", image_bytes=bb)
+    got = host(packed)
+    assert_bytes_equal(got, want_packed, f"{name} load", image_bytes=bb)
+    assert (got[n * bb:] == 0xEE).all(), f"{name} load wrote past the packed buffer"
+    packed = packed[: n * bb]
 
     # gather, tile grid
     grid_h = oracle.grid_coords(v)
-    packed_g = dev_empty(len(grid_h) * bb, fill=0xEE)
+    packed_g = dev_empty(len(grid_h) * bb + guard, fill=0xEE)
     atb.tile_load(ms, None, 0, packed_g, **launch)
     device_ok(atb)
-    assert_bytes_equal(host(packed_g), oracle.tile_load(v, src_h, grid_h), f"{name} grid load", image_bytes=bb)
+    got_g = host(packed_g)
+    assert_bytes_equal(got_g, oracle.tile_load(v, src_h, grid_h), f"{name} grid load", image_bytes=bb)
+    assert (got_g[len(grid_h) * bb:] == 0xEE).all(), f"{name} grid load wrote past the packed buffer"
 
     # scatter of random images to listed origins (later boxes overwrite earlier
     # ones where they overlap, so use disjoint-content-free check: one box per
     # call sequence is order-free only without overlap -> use the grid here)
     images_h = datagen.random_bytes(len(grid_h) * bb, 7)
     images = dev_bytes(images_h)
-    out = dev_empty(nbytes, fill=0x5A)
+    out = dev_empty(nbytes + guard, fill=0x5A)  # bytes past the tensor must stay 0x5A
     md = atb.encode_tiled(dtype, out, dims, v.strides, box, swizzle)
     atb.tile_store(md, None, 0, images, **launch)
     device_ok(atb)
-    want = np.full(nbytes, 0x5A, dtype=np.uint8)
+    want = np.full(nbytes + guard, 0x5A, dtype=np.uint8)
     oracle.tile_store(v, want, grid_h, images_h)
     assert_bytes_equal(host(out), want, f"{name} grid store")
 
     # listed origins, overlapping boxes carry identical bytes (images of a load)
-    out2 = dev_empty(nbytes, fill=0x5A)
+    out2 = dev_empty(nbytes + guard, fill=0x5A)
     md2 = atb.encode_tiled(dtype, out2, dims, v.strides, box, swizzle)
     atb.tile_store(md2, coords, n, packed, **launch)
     device_ok(atb)
-    want2 = np.full(nbytes, 0x5A, dtype=np.uint8)
+    want2 = np.full(nbytes + guard, 0x5A, dtype=np.uint8)
     oracle.tile_store(v, want2, coords_h, want_packed)
     assert_bytes_equal(host(out2), want2, f"{name} listed store")
 
     # round trip with listed origins into a prefilled tensor
-    out3 = dev_empty(nbytes, fill=0x33)
+    out3 = dev_empty(nbytes + guard, fill=0x33)
     md3 = atb.encode_tiled(dtype, out3, dims, v.strides, box, swizzle)
     atb.tile_roundtrip(ms, md3, coords, n, **launch)
     device_ok(atb)
-    want3 = np.full(nbytes, 0x33, dtype=np.uint8)
+    want3 = np.full(nbytes + guard, 0x33, dtype=np.uint8)
     oracle.roundtrip(v, src_h, v, want3, coords_h)
     assert_bytes_equal(host(out3), want3, f"{name} roundtrip")
 
@@ -512,27 +518,30 @@ def test_traversal_steps_all_ops(atb, case):
     bb = atb.box_bytes(ms)
     assert bb == oracle.box_bytes(v)
     n = len(coords_h)
-    packed = dev_empty(n * bb, fill=0xEE)
+    guard = 4096  # bytes past the packed images and past the tensor must survive
+    packed = dev_empty(n * bb + guard, fill=0xEE)
     atb.tile_load(ms, coords, n, packed)
     device_ok(atb)
     want_packed = oracle.tile_load(v, src_h, coords_h)
-    assert_bytes_equal(host(packed), want_packed, f"{name} load", image_bytes=bb)
+    got = host(packed)
+    assert_bytes_equal(got, want_packed, f"{name} load", image_bytes=bb)
+    assert (got[n * bb:] == 0xEE).all(), f"{name} load wrote past the packed buffer"
 
     grid_h = oracle.grid_coords(v)
     images_h = datagen.random_bytes(len(grid_h) * bb, 902)
-    out = dev_empty(nbytes, fill=0x5A)
+    out = dev_empty(nbytes + guard, fill=0x5A)
     md = atb.encode_tiled(dtype, out, dims, strides, box, swizzle, elem_strides=steps)
     atb.tile_store(md, None, 0, dev_bytes(images_h))
     device_ok(atb)
-    want = np.full(nbytes, 0x5A, dtype=np.uint8)
+    want = np.full(nbytes + guard, 0x5A, dtype=np.uint8)
     oracle.tile_store(v, want, grid_h, images_h)
     assert_bytes_equal(host(out), want, f"{name} grid store")
 
-    out2 = dev_empty(nbytes, fill=0x33)
+    out2 = dev_empty(nbytes + guard, fill=0x33)
     md2 = atb.encode_tiled(dtype, out2, dims, strides, box, swizzle, elem_strides=steps)
     atb.tile_roundtrip(ms, md2, coords, n)
     device_ok(atb)
-    want2 = np.full(nbytes, 0x33, dtype=np.uint8)
+    want2 = np.full(nbytes + guard, 0x33, dtype=np.uint8)
     oracle.roundtrip(v, src_h, v, want2, coords_h)
     assert_bytes_equal(host(out2), want2, f"{name} listed round trip")
 

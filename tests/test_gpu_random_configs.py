@@ -80,33 +80,38 @@ def test_random_configuration(atb, seed):
     n = c["n"]
     what = f"case {c}"
 
-    packed = dev_empty(n * bb, fill=0xEE)
+    guard = 4096  # bytes past every destination must keep their fill
+    packed = dev_empty(n * bb + guard, fill=0xEE)
     atb.tile_load(ms, coords, n, packed, **c["launch"])
     want_packed = oracle.tile_load(v, src_h, coords_h)
     assert atb.device_status().code == 0
-    assert_bytes_equal(host(packed), want_packed, "listed gather " + what, image_bytes=bb)
+    got = host(packed)
+    assert_bytes_equal(got, want_packed, "listed gather " + what, image_bytes=bb)
+    assert (got[n * bb:] == 0xEE).all(), "listed gather wrote past its buffer " + what
 
     grid_h = oracle.grid_coords(v)
-    packed_g = dev_empty(len(grid_h) * bb, fill=0xEE)
+    packed_g = dev_empty(len(grid_h) * bb + guard, fill=0xEE)
     atb.tile_load(ms, None, 0, packed_g, **c["launch"])
     assert atb.device_status().code == 0
-    assert_bytes_equal(host(packed_g), oracle.tile_load(v, src_h, grid_h), "grid gather " + what, image_bytes=bb)
+    got_g = host(packed_g)
+    assert_bytes_equal(got_g, oracle.tile_load(v, src_h, grid_h), "grid gather " + what, image_bytes=bb)
+    assert (got_g[len(grid_h) * bb:] == 0xEE).all(), "grid gather wrote past its buffer " + what
 
-    out = dev_empty(c["nbytes"], fill=0x5A)
+    out = dev_empty(c["nbytes"] + guard, fill=0x5A)
     md = atb.encode_tiled(c["dtype"], out, c["dims"], c["strides"], c["box"], c["swizzle"],
                           elem_strides=c["steps"])
     atb.tile_store(md, coords, n, packed, **c["launch"])
     assert atb.device_status().code == 0
-    want = np.full(c["nbytes"], 0x5A, dtype=np.uint8)
+    want = np.full(c["nbytes"] + guard, 0x5A, dtype=np.uint8)
     oracle.tile_store(v, want, coords_h, want_packed)
     assert_bytes_equal(host(out), want, "listed store " + what)
 
-    out2 = dev_empty(c["nbytes"], fill=0x33)
+    out2 = dev_empty(c["nbytes"] + guard, fill=0x33)
     md2 = atb.encode_tiled(c["dtype"], out2, c["dims"], c["strides"], c["box"], c["swizzle"],
                            elem_strides=c["steps"])
     atb.tile_roundtrip(ms, md2, coords, n, **c["launch"])
     assert atb.device_status().code == 0
-    want2 = np.full(c["nbytes"], 0x33, dtype=np.uint8)
+    want2 = np.full(c["nbytes"] + guard, 0x33, dtype=np.uint8)
     oracle.roundtrip(v, src_h, v, want2, coords_h)
     assert_bytes_equal(host(out2), want2, "listed round trip " + what)
 
