@@ -75,6 +75,8 @@ def _load():
         lib.oracle_grid_coords.restype = None
         lib.oracle_tile_load.argtypes = [P, u8p, u8p, ctypes.c_uint64, u8p]
         lib.oracle_tile_load.restype = None
+        lib.oracle_tile_oob_mask.argtypes = [P, u8p, ctypes.c_uint64, u8p]
+        lib.oracle_tile_oob_mask.restype = None
         lib.oracle_tile_store.argtypes = [P, u8p, u8p, ctypes.c_uint64, u8p]
         lib.oracle_tile_store.restype = None
         lib.oracle_roundtrip.argtypes = [P, u8p, P, u8p, u8p, ctypes.c_uint64]
@@ -168,6 +170,16 @@ def tile_load(v: View, base: np.ndarray, coords: np.ndarray) -> np.ndarray:
     out = np.empty(c.shape[0] * box_bytes(v), dtype=np.uint8)
     if c.shape[0]:
         _load().oracle_tile_load(ctypes.byref(v._c()), _ptr(base), _ptr(c), c.shape[0], _ptr(out))
+    return out
+
+
+def tile_oob_mask(v: View, coords: np.ndarray) -> np.ndarray:
+    """Per byte of the packed images of ``tile_load``: 1 where the element lies
+    outside the tensor (the bytes a load fills), else 0."""
+    c = _coords(coords, v)
+    out = np.empty(c.shape[0] * box_bytes(v), dtype=np.uint8)
+    if c.shape[0]:
+        _load().oracle_tile_oob_mask(ctypes.byref(v._c()), _ptr(c), c.shape[0], _ptr(out))
     return out
 
 

@@ -30,6 +30,10 @@
  *   R5  a traversal step e along an outer dimension makes the box visit every
  *       e-th element of its extent (ceil(box / e) elements), packed densely in
  *       the image; the tile grid still advances by the box extent.
+ *   R6  with the NaN fill the descriptor can request instead of zeros, an
+ *       out-of-bounds load element reads as some NaN of the element type; no
+ *       page gives the bit pattern, so the oracle names the filled bytes
+ *       (oracle_tile_oob_mask) rather than their values.
  *
  * Parity of every function is pinned by tests that do not re-type these
  * formulas: the byte counts and tile positions the pages print, brute-force
@@ -166,6 +170,31 @@ void oracle_tile_load(const oracle_view* v, const uint8_t* base,
             for (int32_t b = 0; b < v->esize; ++b) {
                 uint64_t o = e * (uint64_t)v->esize + (uint64_t)b;
                 image[oracle_swizzle(o, v->swizzle_bits)] = inside ? base[addr + (uint64_t)b] : 0;
+            }
+        }
+    }
+}
+
+/*
+ * Which image bytes a load fills rather than reads: [ARC] "The architecture:
+ * every piece explained" (the engine fills what lies outside the tensor) and
+ * reading R6.  Same walk as the load, recording "outside" at the swizzled
+ * position of each byte of each element.
+ */
+void oracle_tile_oob_mask(const oracle_view* v, const int32_t* coords, uint64_t n,
+                          uint8_t* mask)
+{
+    uint64_t box_bytes = oracle_box_bytes(v);
+    uint64_t box_elems = box_bytes / (uint64_t)v->esize;
+    int64_t g[ORACLE_MAX_RANK];
+    for (uint64_t i = 0; i < n; ++i) {
+        const int32_t* c = coords + i * (uint64_t)v->rank;
+        uint8_t* image = mask + i * box_bytes;
+        for (uint64_t e = 0; e < box_elems; ++e) {
+            uint8_t outside = element_in_bounds(v, c, e, g) ? 0 : 1;
+            for (int32_t b = 0; b < v->esize; ++b) {
+                uint64_t o = e * (uint64_t)v->esize + (uint64_t)b;
+                image[oracle_swizzle(o, v->swizzle_bits)] = outside;
             }
         }
     }

@@ -55,6 +55,13 @@ void oracle_grid_coords(const oracle_view* v, int32_t* coords);
 void oracle_tile_load(const oracle_view* v, const uint8_t* base,
                       const int32_t* coords, uint64_t n, uint8_t* packed);
 
+/* Marks, for n boxes, which bytes of each packed image belong to elements
+ * outside the tensor: mask[i*box_bytes + swizzled offset] = 1 for every byte
+ * of an out-of-bounds element, 0 otherwise.  These are the bytes a load fills
+ * instead of reading. */
+void oracle_tile_oob_mask(const oracle_view* v, const int32_t* coords, uint64_t n,
+                          uint8_t* mask);
+
 /* Scatter n packed box images back to the tensor; out-of-bounds elements are skipped. */
 void oracle_tile_store(const oracle_view* v, uint8_t* base,
                        const int32_t* coords, uint64_t n, const uint8_t* packed);

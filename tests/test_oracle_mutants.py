@@ -30,6 +30,9 @@ MUTANTS = {
     "traversal_step_ignored": ("g[d] = (int64_t)c[d] + k * (int64_t)step_along(v, d);", "g[d] = (int64_t)c[d] + k;"),
     "store_unswizzled": ("base[addr + (uint64_t)b] = image[oracle_swizzle(o, v->swizzle_bits)];",
                          "base[addr + (uint64_t)b] = image[o];"),
+    "oob_mask_unswizzled": ("image[oracle_swizzle(o, v->swizzle_bits)] = outside;", "image[o] = outside;"),
+    "oob_mask_inverted": ("uint8_t outside = element_in_bounds(v, c, e, g) ? 0 : 1;",
+                          "uint8_t outside = element_in_bounds(v, c, e, g) ? 1 : 0;"),
     "add_subtracts": ("x = x + addend;", "x = x - addend;"),
     "roundtrip_skips_store": ("    oracle_tile_store(dst, dst_base, coords, n, packed);\n    free(packed);\n    return 0;\n}\n\n/*",
                               "    free(packed);\n    return 0;\n}\n\n/*"),

@@ -438,3 +438,51 @@ def test_store_with_steps_writes_only_visited_elements():
                 np.testing.assert_array_equal(a[y], img[i, k])
     untouched = [y for y in range(rows) if (y % 8) % 3 != 0 or (y % 8) > 6]
     assert (base.reshape(rows, 128)[untouched] == 0x11).all()
+
+
+# --------------------------------------------------------------------------
+# out-of-bounds mask (the bytes a NaN-filling load fills instead of reading)
+# --------------------------------------------------------------------------
+def np_inside_image(v: oracle.View, origin, mode: str) -> np.ndarray:
+    """1 per image byte whose element is inside the tensor, by numpy: a buffer
+    of ones seen through the view, zero-padded, sliced with the steps, then
+    placed by the chunk rules."""
+    ones = np.ones(v.span_bytes(), dtype=np.uint8)
+    return swizzle_image(np_box_stepped(ones, v, origin).reshape(-1), mode)
+
+
+@pytest.mark.parametrize("mode,steps", [("none", (1, 1)), ("128B", (1, 1)), ("64B", (1, 3)), ("32B", (1, 2))])
+def test_oob_mask_brute_force(mode, steps):
+    esize = 4
+    inner = {"none": 12, "32B": 8, "64B": 16, "128B": 32}[mode]
+    rows, cols = 19, inner * 2 + 4
+    v = oracle.View(esize, (cols, rows), (esize, cols * esize + 16), (inner, 7), mode, steps)
+    origins = np.array([(x, y) for y in range(-7, 20, 3) for x in range(-inner, cols + 1, 4)], dtype=np.int32)
+    mask = oracle.tile_oob_mask(v, origins)
+    bb = oracle.box_bytes(v)
+    assert mask.size == len(origins) * bb and set(np.unique(mask)) <= {0, 1}
+    for i, o in enumerate(origins):
+        np.testing.assert_array_equal(mask[i * bb:(i + 1) * bb], 1 - np_inside_image(v, o, mode),
+                                      err_msg=f"origin {o}")
+
+
+def test_oob_mask_c3_edge_tiles_closed_form():
+    w = datagen.C3
+    v = oracle.View(*_c(w))
+    coords = oracle.grid_coords(v)
+    pick = [0, int(np.nonzero(coords[:, 1] == 78 * 128)[0][0]), int(np.nonzero(coords[:, 0] == 46 * 64)[0][0]),
+            len(coords) - 1]
+    mask = oracle.tile_oob_mask(v, coords[pick]).reshape(4, -1)
+    valid_rows, valid_cols = 16, 56
+    assert mask[0].sum() == 0
+    assert mask[1].sum() == (128 - valid_rows) * 64 * 2
+    assert mask[2].sum() == 128 * (64 - valid_cols) * 2
+    assert mask[3].sum() == (128 * 64 - valid_rows * valid_cols) * 2
+
+
+def test_oob_mask_marks_whole_elements_and_a_box_outside_is_all_fill():
+    v = oracle.View(8, (6, 5), (8, 48), (4, 4), "none")
+    mask = oracle.tile_oob_mask(v, np.array([[4, 3], [-4, 0], [0, 5]], dtype=np.int32)).reshape(3, 4, 4, 8)
+    assert ((mask.min(axis=3) == mask.max(axis=3))).all()  # all 8 bytes of an element agree
+    assert mask[1].all() and mask[2].all()  # entirely left of / below the tensor
+    np.testing.assert_array_equal(mask[0, :, :, 0], [[0, 0, 1, 1], [0, 0, 1, 1], [1, 1, 1, 1], [1, 1, 1, 1]])
