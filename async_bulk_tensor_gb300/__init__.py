@@ -34,6 +34,7 @@ for _i, _n in enumerate(STATUS):
 DTYPES = {"u8": 0, "u16": 1, "u32": 2, "i32": 3, "u64": 4, "i64": 5, "f16": 6, "f32": 7, "f64": 8, "bf16": 9}
 SWIZZLES = {"none": 0, "32B": 1, "64B": 2, "128B": 3}
 L2_PROMOTIONS = {"none": 0, "64B": 1, "128B": 2, "256B": 3}
+OOB_FILLS = {"zero": 0, "nan": 1}
 SCHEDULES = {"strided": 0, "contiguous": 1}
 
 
@@ -184,10 +185,11 @@ def status_string(code: int) -> str:
 
 
 def encode_tiled(dtype: str, base, dims, strides_bytes, box, swizzle="none", l2_promotion="none",
-                 elem_strides=None) -> TensorMap:
+                 elem_strides=None, oob_fill="zero") -> TensorMap:
     """Encode a tiled tensor map (``atb_encode_tiled``); sequences are innermost first.
 
     ``strides_bytes`` lists a byte stride per dimension; entry 0 is ignored.
+    ``oob_fill`` is "zero" or "nan" (floating-point types only).
     """
     rank = len(dims)
     m = TensorMap()
@@ -198,7 +200,8 @@ def encode_tiled(dtype: str, base, dims, strides_bytes, box, swizzle="none", l2_
     code = lib.atb_encode_tiled(ctypes.byref(m), DTYPES[dtype] if isinstance(dtype, str) else dtype, rank,
                                 _ptr(base), a_dims, a_str, a_box, a_es,
                                 SWIZZLES[swizzle] if isinstance(swizzle, str) else swizzle,
-                                L2_PROMOTIONS[l2_promotion] if isinstance(l2_promotion, str) else l2_promotion, 0)
+                                L2_PROMOTIONS[l2_promotion] if isinstance(l2_promotion, str) else l2_promotion,
+                                OOB_FILLS[oob_fill] if isinstance(oob_fill, str) else oob_fill)
     _check(code, "atb_encode_tiled")
     return m
 

@@ -124,6 +124,11 @@ uint32_t dtype_size(uint32_t dt)
     }
 }
 
+bool dtype_is_float(uint32_t dt)
+{
+    return dt == ATB_F16 || dt == ATB_BF16 || dt == ATB_F32 || dt == ATB_F64;
+}
+
 CUtensorMapDataType dtype_to_cu(uint32_t dt)
 {
     switch (dt) {
@@ -267,7 +272,11 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
     }
     if (static_cast<uint32_t>(l2_promotion) > ATB_L2_PROMO_256B)
         return set_error(ATB_ERR_ARG, "unknown L2 promotion %d", static_cast<int>(l2_promotion));
-    if (oob_fill != ATB_OOB_ZERO) return set_error(ATB_ERR_ARG, "only zero out-of-bounds fill is supported");
+    if (oob_fill != ATB_OOB_ZERO && oob_fill != ATB_OOB_NAN)
+        return set_error(ATB_ERR_ARG, "unknown out-of-bounds fill %d", static_cast<int>(oob_fill));
+    if (oob_fill == ATB_OOB_NAN && !dtype_is_float(static_cast<uint32_t>(dtype)))
+        return set_error(ATB_ERR_DTYPE, "NaN out-of-bounds fill needs a floating-point element type, not dtype %d",
+                         static_cast<int>(dtype));
 
     uint64_t box_bytes = esize;
     for (uint32_t d = 0; d < rank; ++d) box_bytes *= (box[d] + steps[d] - 1) / steps[d];
@@ -291,7 +300,9 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
     alignas(64) CUtensorMap map;
     CUresult r = fn(&map, dtype_to_cu(dtype), rank, gbase, gdim, gstride, bdim, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(swizzle),
-                    static_cast<CUtensorMapL2promotion>(l2_promotion), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    static_cast<CUtensorMapL2promotion>(l2_promotion),
+                    oob_fill == ATB_OOB_NAN ? CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA
+                                            : CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return set_error(ATB_ERR_DRIVER, "cuTensorMapEncodeTiled refused the map (CUresult %d)", static_cast<int>(r));
 

@@ -98,8 +98,16 @@ typedef enum {
     ATB_L2_PROMO_NONE = 0, ATB_L2_PROMO_64B = 1, ATB_L2_PROMO_128B = 2, ATB_L2_PROMO_256B = 3
 } atb_l2_promotion;
 
+/*
+ * What a load puts in the image for elements outside the tensor ([ARC] "The
+ * architecture: every piece explained": the descriptor carries the boundary
+ * handling).  Stores never write outside the tensor, whatever the fill.
+ */
 typedef enum {
-    ATB_OOB_ZERO = 0             /* out-of-bounds load elements read as zero bytes */
+    ATB_OOB_ZERO = 0,            /* out-of-bounds load elements read as zero bytes */
+    ATB_OOB_NAN = 1              /* floating-point types only (f16, bf16, f32, f64): they read as
+                                    a NaN of the element type, the driver's NaN-request-zero-FMA
+                                    fill; the bit pattern is the hardware's */
 } atb_oob_fill;
 
 /*
@@ -195,6 +203,8 @@ const char* atb_last_error(void);
  *   swizzle known                                -> ATB_ERR_SWIZZLE
  *   swizzled: box[0] * element size == span (32/64/128) -> ATB_ERR_SWIZZLE_SPAN
  *   elem_strides NULL, or [0] == 1 and each entry in 1..8 -> ATB_ERR_ARG
+ *   l2_promotion known, oob_fill known           -> ATB_ERR_ARG
+ *   oob_fill ATB_OOB_NAN with an integer dtype    -> ATB_ERR_DTYPE
  * then fetches cuTensorMapEncodeTiled through the runtime's driver entry point
  * (no libcuda link) and encodes; a driver refusal -> ATB_ERR_DRIVER.
  *

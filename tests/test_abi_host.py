@@ -84,12 +84,17 @@ def test_encoder_rules_each_have_their_own_status(atb):
     _expect(atb, atb.ATB_ERR_ARG, elem_strides=(2, 1))  # no step along the contiguous dimension
     _expect(atb, atb.ATB_ERR_ARG, elem_strides=(1, 9))  # steps are 1..8
     _expect(atb, atb.ATB_ERR_ARG, elem_strides=(1, 0))
+    _expect(atb, atb.ATB_ERR_ARG, oob_fill=7)
+    for integer in ("u8", "u16", "u32", "i32", "u64", "i64"):  # the NaN fill is for floating-point types
+        msg = _expect(atb, atb.ATB_ERR_DTYPE, dtype=integer, box=(64, 16), oob_fill="nan")
+        assert "NaN" in msg
 
 
 def test_valid_map_reaches_the_driver(atb):
     # With no GPU driver the entry point is unavailable; on a GPU the map encodes.
     try:
         m = atb.encode_tiled("f16", 0x10000, (1024, 64), (2, 2048), (64, 16))
+        atb.encode_tiled("bf16", 0x10000, (1024, 64), (2, 2048), (64, 16), oob_fill="nan")
     except atb.AtbError as e:
         assert e.code == atb.ATB_ERR_DRIVER
     else:

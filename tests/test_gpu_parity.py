@@ -658,3 +658,114 @@ def test_cuda_graph_capture_and_replay(atb):
         want = np.zeros_like(new_h)
         oracle.roundtrip(v, new_h, v, want, oracle.grid_coords(v))
         assert_bytes_equal(host(out), want, f"graph round trip {seed}")
+
+
+# --------------------------------------------------------------------------
+# NaN out-of-bounds fill: in-bounds bytes exact, every filled element a NaN
+# --------------------------------------------------------------------------
+def _is_nan_bits(img: np.ndarray, dtype: str) -> np.ndarray:
+    """Per element of the images: is it a NaN of ``dtype`` (by its bit fields)."""
+    if dtype in ("f16", "bf16"):
+        x = img.view(np.uint16)
+        exp, man = (0x7C00, 0x03FF) if dtype == "f16" else (0x7F80, 0x007F)
+    elif dtype == "f32":
+        x, exp, man = img.view(np.uint32), 0x7F800000, 0x007FFFFF
+    else:
+        x, exp, man = img.view(np.uint64), 0x7FF0000000000000, 0x000FFFFFFFFFFFFF
+    return ((x & x.dtype.type(exp)) == exp) & ((x & x.dtype.type(man)) != 0)
+
+
+def _check_nan_fill(got: np.ndarray, v: oracle.View, src_h, coords_h, dtype, what):
+    want = oracle.tile_load(v, src_h, coords_h)  # zero fill: right wherever the mask is 0
+    mask = oracle.tile_oob_mask(v, coords_h)
+    got = got[: want.size]
+    inside = mask == 0
+    bad = np.flatnonzero(got[inside] != want[inside])
+    assert bad.size == 0, f"{what}: {bad.size} in-bounds bytes differ"
+    elem_out = mask.reshape(-1, v.esize)[:, 0] == 1
+    assert elem_out.any(), f"{what}: the case has no out-of-bounds element"
+    nan = _is_nan_bits(got, dtype)
+    assert nan[elem_out].all(), f"{what}: {int((~nan[elem_out]).sum())} filled elements are not NaN"
+
+
+NAN_CASES = [c for c in SMALL if c[1] in ("f16", "bf16", "f32", "f64")]
+
+
+@pytest.mark.parametrize("case", NAN_CASES, ids=[c[0] for c in NAN_CASES])
+def test_nan_fill_gather_and_round_trip(atb, case):
+    name, dtype, dims, box, swizzle, order = case
+    v, src_h, nbytes, coords_h = _small_case(name, dtype, dims, box, swizzle, order, 3000 + len(name))
+    launch = dict(stages=1) if box == (256, 256) else {}
+    src = dev_bytes(src_h)
+    coords = dev_bytes(coords_h.view(np.uint8))
+    ms = atb.encode_tiled(dtype, src, dims, v.strides, box, swizzle, oob_fill="nan")
+    bb = atb.box_bytes(ms)
+    n = coords_h.shape[0]
+
+    packed = dev_empty(n * bb, fill=0)
+    atb.tile_load(ms, coords, n, packed, **launch)
+    device_ok(atb)
+    _check_nan_fill(host(packed), v, src_h, coords_h, dtype, f"{name} listed gather")
+
+    grid_h = oracle.grid_coords(v)
+    packed_g = dev_empty(len(grid_h) * bb, fill=0)
+    atb.tile_load(ms, None, 0, packed_g, **launch)
+    device_ok(atb)
+    if (oracle.tile_oob_mask(v, grid_h) == 1).any():
+        _check_nan_fill(host(packed_g), v, src_h, grid_h, dtype, f"{name} grid gather")
+    else:
+        assert_bytes_equal(host(packed_g), oracle.tile_load(v, src_h, grid_h), f"{name} grid gather")
+
+    # a store never writes outside the tensor, so the fill cannot reach the output
+    out = dev_empty(nbytes, fill=0x33)
+    md = atb.encode_tiled(dtype, out, dims, v.strides, box, swizzle, oob_fill="nan")
+    atb.tile_roundtrip(ms, md, coords, n, **launch)
+    device_ok(atb)
+    want = np.full(nbytes, 0x33, dtype=np.uint8)
+    oracle.roundtrip(v, src_h, v, want, coords_h)
+    assert_bytes_equal(host(out), want, f"{name} round trip")
+
+
+def test_nan_fill_workload3_edges_and_steps(atb):
+    # ragged 10000 x 3000 bf16, 128-byte swizzle: NaN exactly where the edge boxes overhang
+    w = datagen.C3
+    v = oracle_view(w)
+    src_h = datagen.storage(w)
+    src = dev_bytes(src_h)
+    ms = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle, oob_fill="nan")
+    grid_h = oracle.grid_coords(v)
+    packed = dev_empty(len(grid_h) * atb.box_bytes(ms), fill=0)
+    atb.tile_load(ms, None, 0, packed)
+    device_ok(atb)
+    _check_nan_fill(host(packed), v, src_h, grid_h, "bf16", "workload 3 grid gather")
+
+    # traversal steps with the NaN fill: f32, step 3 along rows
+    dims, box, steps = (200, 77), (32, 10), (1, 3)
+    strides, nbytes = _strides(4, dims)
+    vs = oracle.View(4, dims, strides, box, "128B", steps)
+    s_h = datagen.random_bytes(nbytes, 3100)
+    c_h = datagen.random_box_origins(dims, box, 4, 80, 3101)
+    s_d = dev_bytes(s_h)  # keep the source alive while the map is in use
+    m = atb.encode_tiled("f32", s_d, dims, strides, box, "128B", elem_strides=steps, oob_fill="nan")
+    p = dev_empty(len(c_h) * atb.box_bytes(m), fill=0)
+    atb.tile_load(m, dev_bytes(c_h.view(np.uint8)), len(c_h), p)
+    device_ok(atb)
+    _check_nan_fill(host(p), vs, s_h, c_h, "f32", "stepped gather")
+
+
+def test_nan_fill_fp32_update_matches_zero_fill(atb):
+    # the +1.0f update sees NaN + 1 in the overhang, which the clipped store drops
+    dims, box = (300, 70), (32, 16)
+    strides, nbytes = _strides(4, dims)
+    v = oracle.View(4, dims, strides, box, "128B")
+    src_h = datagen.finite_f32_bytes(nbytes // 4, 3200)
+    coords_h = datagen.random_box_origins(dims, box, 4, 120, 3201)
+    src = dev_bytes(src_h)  # keep the source alive while the map is in use
+    ms = atb.encode_tiled("f32", src, dims, strides, box, "128B", oob_fill="nan")
+    out = dev_empty(nbytes, fill=0x44)
+    md = atb.encode_tiled("f32", out, dims, strides, box, "128B", oob_fill="nan")
+    atb.tile_roundtrip_add_f32(ms, md, 1.0, dev_bytes(coords_h.view(np.uint8)), len(coords_h))
+    device_ok(atb)
+    want = np.full(nbytes, 0x44, dtype=np.uint8)
+    oracle.roundtrip_add_f32(v, src_h, v, want, coords_h, 1.0)
+    assert_bytes_equal(host(out), want, "fp32 update with NaN fill")
