@@ -769,3 +769,87 @@ def test_nan_fill_fp32_update_matches_zero_fill(atb):
     want = np.full(nbytes, 0x44, dtype=np.uint8)
     oracle.roundtrip_add_f32(v, src_h, v, want, coords_h, 1.0)
     assert_bytes_equal(host(out), want, "fp32 update with NaN fill")
+
+
+# --------------------------------------------------------------------------
+# ordering: dependent calls back to back, and independent calls on several streams
+# --------------------------------------------------------------------------
+def _c4_finite():
+    """Workload 4's permuted fp32 view over finite values (the fp32 update is
+    compared bit for bit, which NaN payloads would not allow)."""
+    w = datagen.C4
+    return w, oracle_view(w), datagen.finite_f32_bytes(w.storage_bytes // 4, 4400)
+
+
+def test_dependent_calls_back_to_back_without_host_sync(atb):
+    # each call reads what the previous one wrote; the kernels overlap their
+    # set-up with the previous grid (programmatic dependent launch) and must
+    # still see its writes
+    torch = torch_cuda()
+    w, v, src_h = _c4_finite()
+    coords_h = datagen.workload_coords(w)
+    n = len(coords_h)
+    src, coords = dev_bytes(src_h), dev_bytes(coords_h.view(np.uint8))
+    packed = dev_empty(n * 8192, fill=0)
+    fresh = dev_empty(w.storage_bytes, fill=0x3F)  # 0x3F3F3F3F is a finite fp32
+    out2 = dev_empty(w.storage_bytes, fill=0)
+    out3 = dev_empty(w.storage_bytes, fill=0)
+    packed2 = dev_empty(n * 8192, fill=0)
+    m_src, m_fresh, m_out2, m_out3 = (encode(atb, w, t) for t in (src, fresh, out2, out3))
+    torch.cuda.synchronize()
+    atb.tile_load(m_src, coords, n, packed)                    # 1 gather
+    atb.tile_store(m_fresh, coords, n, packed)                 # 2 reads 1
+    atb.tile_roundtrip(m_fresh, m_out2)                        # 3 reads 2 (whole grid)
+    atb.tile_roundtrip_add_f32(m_out2, m_out3, 1.0)            # 4 reads 3
+    atb.tile_load(m_out3, coords, n, packed2, stages=2)        # 5 reads 4
+    device_ok(atb)
+
+    want_packed = oracle.tile_load(v, src_h, coords_h)
+    want_fresh = np.full(w.storage_bytes, 0x3F, dtype=np.uint8)
+    oracle.tile_store(v, want_fresh, coords_h, want_packed)
+    grid = oracle.grid_coords(v)
+    want2 = np.zeros(w.storage_bytes, dtype=np.uint8)
+    oracle.roundtrip(v, want_fresh, v, want2, grid)
+    want3 = np.zeros(w.storage_bytes, dtype=np.uint8)
+    oracle.roundtrip_add_f32(v, want2, v, want3, grid, 1.0)
+    assert_bytes_equal(host(fresh), want_fresh, "step 2 store")
+    assert_bytes_equal(host(out3), want3, "step 4 fp32 update")
+    assert_bytes_equal(host(packed2), oracle.tile_load(v, want3, coords_h), "step 5 gather", image_bytes=8192)
+
+
+def test_independent_calls_on_four_streams(atb):
+    torch = torch_cuda()
+    w2, w3 = datagen.C2, datagen.C3
+    s2_h, s3_h = datagen.storage(w2, seed=4501), datagen.storage(w3, seed=4502)
+    w4, v4, s4_h = _c4_finite()
+    c4_h = datagen.workload_coords(w4)
+    src2, dst2 = dev_bytes(s2_h), dev_empty(w2.storage_bytes, fill=0)
+    src3 = dev_bytes(s3_h)
+    packed3 = dev_empty(3713 * 16384, fill=0)
+    src4, c4 = dev_bytes(s4_h), dev_bytes(c4_h.view(np.uint8))
+    packed4 = dev_empty(len(c4_h) * 8192, fill=0)
+    out4 = dev_empty(w4.storage_bytes, fill=0x3F)
+    upd = dev_empty(w4.storage_bytes, fill=0)
+    maps = dict(s2=encode(atb, w2, src2), d2=encode(atb, w2, dst2), s3=encode(atb, w3, src3),
+                s4=encode(atb, w4, src4), o4=encode(atb, w4, out4), u=encode(atb, w4, upd))
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    torch.cuda.synchronize()
+    atb.tile_roundtrip(maps["s2"], maps["d2"], stream=streams[0])
+    atb.tile_load(maps["s3"], None, 0, packed3, stream=streams[1])
+    atb.tile_load(maps["s4"], c4, len(c4_h), packed4, stream=streams[2])
+    atb.tile_store(maps["o4"], c4, len(c4_h), packed4, stream=streams[2])
+    atb.tile_roundtrip_add_f32(maps["s4"], maps["u"], -2.5, stream=streams[3])
+    torch.cuda.synchronize()
+    device_ok(atb)
+
+    assert_bytes_equal(host(dst2), s2_h, "stream 1 round trip")
+    v3 = oracle_view(w3)
+    assert_bytes_equal(host(packed3), oracle.tile_load(v3, s3_h, oracle.grid_coords(v3)), "stream 2 gather",
+                       image_bytes=16384)
+    want_p4 = oracle.tile_load(v4, s4_h, c4_h)
+    want_o4 = np.full(w4.storage_bytes, 0x3F, dtype=np.uint8)
+    oracle.tile_store(v4, want_o4, c4_h, want_p4)
+    assert_bytes_equal(host(out4), want_o4, "stream 3 gather then store")
+    want_u = np.zeros(w4.storage_bytes, dtype=np.uint8)
+    oracle.roundtrip_add_f32(v4, s4_h, v4, want_u, oracle.grid_coords(v4), -2.5)
+    assert_bytes_equal(host(upd), want_u, "stream 4 fp32 update")
