@@ -27,6 +27,7 @@ STATUS = [
     "ATB_ERR_SMEM_ALIGN", "ATB_ERR_SWIZZLE", "ATB_ERR_SWIZZLE_SPAN", "ATB_ERR_INNER_BYTES", "ATB_ERR_DTYPE",
     "ATB_ERR_DRIVER", "ATB_ERR_UNSUPPORTED_DEVICE", "ATB_ERR_SMEM_BUDGET", "ATB_ERR_ARG", "ATB_ERR_TIMEOUT",
     "ATB_ERR_CUDA", "ATB_ERR_COORD_ALIGN", "ATB_ERR_COORD_RANGE", "ATB_ERR_STRIDE_RANGE", "ATB_ERR_DIM_RANGE",
+    "ATB_ERR_RING_CHECK",
 ]
 for _i, _n in enumerate(STATUS):
     globals()[_n] = _i
@@ -36,6 +37,7 @@ SWIZZLES = {"none": 0, "32B": 1, "64B": 2, "128B": 3}
 L2_PROMOTIONS = {"none": 0, "64B": 1, "128B": 2, "256B": 3}
 OOB_FILLS = {"zero": 0, "nan": 1}
 SCHEDULES = {"strided": 0, "contiguous": 1}
+CHECK_RING = 1  # atb_launch.checks: stage bookkeeping check
 
 
 class AtbError(RuntimeError):
@@ -79,7 +81,8 @@ class Launch(ctypes.Structure):
         ("no_pdl", ctypes.c_uint32),
         ("poll_suspend_ns", ctypes.c_uint32),
         ("prefetch_boxes", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32 * 3),
+        ("checks", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32 * 2),
     ]
 
 
@@ -171,9 +174,9 @@ HINT_LOAD_EVICT_FIRST, HINT_STORE_EVICT_FIRST, HINT_STORE_EVICT_LAST = 1, 2, 4
 
 
 def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True,
-            poll_suspend_ns=0, prefetch_boxes=0) -> Launch:
+            poll_suspend_ns=0, prefetch_boxes=0, checks=0) -> Launch:
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
-                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes)
+                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes, checks)
 
 
 def version() -> int:

@@ -34,6 +34,8 @@ enum Where : int32_t {
     kWhereProducerIssue = 3,
     kWhereConsumerIssue = 4,
     kWhereSelftest = 5,
+    kWhereProducerRing = 6,
+    kWhereConsumerRing = 7,
 };
 
 // ---- host helpers (defined in encode.cu) -----------------------------------

@@ -210,6 +210,7 @@ const char* atb_status_string(atb_status s)
     case ATB_ERR_COORD_RANGE: return "ATB_ERR_COORD_RANGE";
     case ATB_ERR_STRIDE_RANGE: return "ATB_ERR_STRIDE_RANGE";
     case ATB_ERR_DIM_RANGE: return "ATB_ERR_DIM_RANGE";
+    case ATB_ERR_RING_CHECK: return "ATB_ERR_RING_CHECK";
     }
     return "ATB_ERR_UNKNOWN";
 }

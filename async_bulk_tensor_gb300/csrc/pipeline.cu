@@ -71,6 +71,7 @@ struct PipeArgs {
     uint32_t l2_hints;      // ATB_HINT_* bits
     uint32_t suspend_ns;    // mbarrier poll suspend-time hint, 0 = hardware default
     uint32_t prefetch;      // boxes ahead to prefetch into L2 (tensor loads), 0 = off
+    uint32_t checks;        // ATB_CHECK_* bits
 };
 
 // Shared-memory control words after the stage ring and the barriers.
@@ -79,6 +80,11 @@ struct Control {
     uint32_t issued;         // boxes whose stage the producer has armed
     uint32_t producer_done;
     uint32_t pad;
+    // ATB_CHECK_RING shadows, per stage: 1 + the CTA-local number of the box
+    // the producer last armed it for, and 1 + (the number of the box the
+    // consumer last released it from, modulo 256); 0 = not used yet.
+    uint32_t filled[kMaxStages];
+    uint32_t freed[kMaxStages];
 };
 
 __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int32_t tile, int32_t where)
@@ -392,6 +398,10 @@ __device__ __forceinline__ void init_ring(const Ring& r)
     r.ctl->abort = 0;
     r.ctl->issued = 0;
     r.ctl->producer_done = 0;
+    for (uint32_t s = 0; s < r.stages; ++s) {
+        r.ctl->filled[s] = 0;
+        r.ctl->freed[s] = 0;
+    }
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
 }
@@ -402,6 +412,33 @@ __device__ __forceinline__ void raise_abort(const PipeArgs& a, const Ring& r, ui
         record_error(a.status, ATB_ERR_TIMEOUT, static_cast<int32_t>(tile), where);
         *r.abort_flag() = 1;
     }
+}
+
+// ATB_CHECK_RING: the releasing consumer thread records which box it is done
+// with before arriving on the stage's empty barrier (whose release order
+// publishes the write to the producer's acquiring wait) ...
+__device__ __forceinline__ void ring_note_freed(const PipeArgs& a, const Ring& r, uint32_t stage, uint32_t box)
+{
+    if (a.checks & ATB_CHECK_RING)
+        *reinterpret_cast<volatile uint32_t*>(&r.ctl->freed[stage]) = (box & 255u) + 1u;
+}
+
+// ... and the producer, after that wait, checks it was the stage's previous box.
+__device__ __forceinline__ void ring_check_freed(const PipeArgs& a, const Ring& r, uint32_t stage, uint32_t k,
+                                                 uint32_t tile)
+{
+    if (!(a.checks & ATB_CHECK_RING) || k < r.stages) return;
+    const uint32_t want = ((k - r.stages) & 255u) + 1u;
+    if (*reinterpret_cast<volatile uint32_t*>(&r.ctl->freed[stage]) != want)
+        record_error(a.status, ATB_ERR_RING_CHECK, static_cast<int32_t>(tile), kWhereProducerRing);
+}
+
+// After its full-barrier wait, the consumer checks the stage holds its k-th box.
+__device__ __forceinline__ void ring_check_filled(const PipeArgs& a, const Ring& r, uint32_t stage, uint32_t k,
+                                                  uint32_t tile)
+{
+    if ((a.checks & ATB_CHECK_RING) && *reinterpret_cast<volatile uint32_t*>(&r.ctl->filled[stage]) != k + 1u)
+        record_error(a.status, ATB_ERR_RING_CHECK, static_cast<int32_t>(tile), kWhereConsumerRing);
 }
 
 // One producer thread: for its k-th box, wait until stage k mod N is free,
@@ -434,6 +471,9 @@ __device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, con
             break;
         }
         const uint32_t t = cur.t;
+        ring_check_freed(a, r, s, k, t);
+        if (a.checks & ATB_CHECK_RING)  // published by the arrive below (release order)
+            *reinterpret_cast<volatile uint32_t*>(&r.ctl->filled[s]) = k + 1u;
         int32_t c[R];
         cur.origin(a, c);
         const int32_t bad = origin_error<R>(a, c);
@@ -490,7 +530,7 @@ struct PendingStores {
         ++count;
     }
 
-    __device__ __forceinline__ void retire(const Ring& r, uint32_t k, uint32_t lag)
+    __device__ __forceinline__ void retire(const PipeArgs& a, const Ring& r, uint32_t k, uint32_t lag)
     {
         uint32_t keep = 0;  // groups younger than `lag` boxes may stay in flight
         for (uint32_t i = 0; i < count; ++i)
@@ -498,6 +538,7 @@ struct PendingStores {
         if (keep == count) return;
         ptx::bulk_wait_read_le(keep);
         for (; count > keep; --count) {
+            ring_note_freed(a, r, static_cast<uint32_t>(stages & 15u), static_cast<uint32_t>(boxes & 255u));
             ptx::mbar_arrive(r.empty(static_cast<uint32_t>(stages & 15u)));
             stages >>= 4;
             boxes >>= 8;
@@ -551,6 +592,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
             break;
         }
         const uint32_t t = cur.t;
+        if (lane == 0) ring_check_filled(a, r, s, k, t);
         int32_t c[R];
         cur.origin(a, c);
         const bool skip = origin_error<R>(a, c) != 0;
@@ -574,9 +616,10 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
                 ptx::bulk_commit();
                 pending.push(s, k);
             } else {
+                ring_note_freed(a, r, s, k);
                 ptx::mbar_arrive(r.empty(s));  // written by the warp, or nothing to write
             }
-            pending.retire(r, k, a.store_lag);
+            pending.retire(a, r, k, a.store_lag);
         }
     }
 
@@ -639,6 +682,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
             failed = true;
             break;
         }
+        if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
         int32_t c[R];
         cur.origin(a, c);
         const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
@@ -666,9 +710,10 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
                 ptx::bulk_commit();
                 pending.push(s, k);
             } else {
+                ring_note_freed(a, r, s, k);
                 ptx::mbar_arrive(r.empty(s));  // written by the threads, or nothing to write
             }
-            pending.retire(r, k, a.store_lag);
+            pending.retire(a, r, k, a.store_lag);
         }
     }
 
@@ -789,6 +834,8 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
             return set_error(ATB_ERR_ARG,
                              "source and destination maps differ in rank, element size, box, steps or swizzle");
     }
+    if (cfg && (cfg->checks & ~ATB_CHECK_RING))
+        return set_error(ATB_ERR_ARG, "unknown check bits 0x%x", cfg->checks & ~ATB_CHECK_RING);
     if (MODE == kLoad || MODE == kStore) {
         if (!packed) return set_error(ATB_ERR_ARG, "packed buffer is NULL");
         if (reinterpret_cast<uintptr_t>(packed) % 16)
@@ -873,6 +920,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.l2_hints = cfg ? cfg->l2_hints : 0u;
     a.suspend_ns = cfg ? cfg->poll_suspend_ns : 0u;
     a.prefetch = cfg ? cfg->prefetch_boxes : 0u;
+    a.checks = cfg ? cfg->checks : 0u;
     a.swizzle_bits = swizzle_bits(shape->swizzle);
     for (uint32_t d = 0; d < rank; ++d) {
         a.box[d] = shape->box[d];

@@ -334,6 +334,9 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
             out[f"{box}_s3_l2promotion{promo}"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
         s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, pdl=False), steps, 5)
         out[f"{box}_s3_without_pdl"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
+        s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, checks=atb.CHECK_RING),
+                          steps, 5)
+        out[f"{box}_s3_ring_check"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
     return out
 
 

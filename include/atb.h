@@ -82,7 +82,9 @@ typedef enum {
     ATB_ERR_COORD_ALIGN = 16,    /* (device) a box origin breaks the 16-byte rule along x */
     ATB_ERR_COORD_RANGE = 17,    /* (device) a box origin is beyond +-2^30 */
     ATB_ERR_STRIDE_RANGE = 18,   /* a byte stride (dims 1..rank-1) is 0 or not below 2^40 */
-    ATB_ERR_DIM_RANGE = 19       /* an extent is 0 or above 2^32 */
+    ATB_ERR_DIM_RANGE = 19,      /* an extent is 0 or above 2^32 */
+    ATB_ERR_RING_CHECK = 20      /* (device, checked launches) a ring stage held another box than
+                                    the one the waiting role expected */
 } atb_status;
 
 typedef enum {
@@ -149,8 +151,29 @@ typedef struct {
     uint32_t poll_suspend_ns; /* mbarrier waits: suspend-time hint per poll in ns (0 = hardware default) */
     uint32_t prefetch_boxes;  /* tensor loads: prefetch the box this many boxes ahead into L2 with
                                  cp.async.bulk.prefetch.tensor (0 = off) */
-    uint32_t reserved[3];
+    uint32_t checks;          /* ATB_CHECK_* bits: consistency checks inside the kernel (0 = none) */
+    uint32_t reserved[2];
 } atb_launch;
+
+/*
+ * atb_launch.checks bits.
+ *
+ * ATB_CHECK_RING  stage bookkeeping check, a debugging aid for the ring (the
+ *   pages' failure modes of a TMA pipeline are silent: a consumer that waits
+ *   on the wrong phase parity reads a stale or half-written box, "Understanding
+ *   TMA loads in CuTe DSL", "Issue the load and wait for its phase"; "Day 76:
+ *   The Tensor Memory Accelerator (TMA)", "Pitfalls").  Each CTA keeps two
+ *   shadow words per stage in shared memory.  Before arming a stage the
+ *   producer writes the number of the box it is about to load there; after its
+ *   full-barrier wait the consumer compares that number with the box it
+ *   expects.  When a stage is released the consumer writes the number of the
+ *   box it is done with; after its empty-barrier wait the producer compares it
+ *   with the stage's previous box.  The barriers' release/acquire order makes
+ *   each shadow write visible to the waiting role.  A mismatch records
+ *   ATB_ERR_RING_CHECK (where = 6 producer, 7 consumer) and the launch goes
+ *   on; no wait is added.  Costs a few shared-memory accesses per box.
+ */
+#define ATB_CHECK_RING 1u
 
 /* atb_launch.l2_hints bits */
 #define ATB_HINT_LOAD_EVICT_FIRST  1u
@@ -163,7 +186,7 @@ typedef struct {
     int32_t block;         /* CTA that recorded it */
     int32_t tile;          /* box index (position in the list or grid) it was working on */
     int32_t where;         /* 1 producer wait, 2 consumer wait, 3 producer issue, 4 consumer issue,
-                              5 self-test wait */
+                              5 self-test wait, 6 producer ring check, 7 consumer ring check */
     uint32_t errors;       /* number of device-side errors recorded since the last reset */
     uint32_t reserved[3];
 } atb_device_report;

@@ -107,3 +107,18 @@ def test_null_maps_are_rejected_without_a_device(atb):
         atb.tile_roundtrip(m, m)
     assert e.value.code == atb.ATB_ERR_ARG
     assert atb.box_bytes(m) == 0 and atb.grid_tiles(m) == 0
+
+
+
+def test_unknown_check_bits_are_rejected_before_any_device_work(atb):
+    # a map record that passes the library's validity check (magic and rank);
+    # the launch must refuse the unknown bit before asking for a device
+    m = atb.TensorMap()
+    m.magic, m.rank, m.esize, m.dtype = 0x31425441, 2, 2, atb.DTYPES["f16"]
+    m.base, m.box_bytes = 0x10000, 2048
+    for d, (n, b) in enumerate(((1024, 64), (64, 16))):
+        m.dims[d], m.box[d], m.elem_strides[d] = n, b, 1
+    m.strides[0], m.strides[1] = 2, 2048
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_roundtrip(m, m, checks=2)
+    assert e.value.code == atb.ATB_ERR_ARG and "check bits" in str(e.value)

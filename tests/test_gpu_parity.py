@@ -145,6 +145,18 @@ def test_c5_full_round_trip_default_launch(atb, w, c5_input, c5_device):
     assert_bytes_equal(host(dst), want, w.name, view=v)
 
 
+@pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
+def test_c5_ring_check_full_size(atb, w, c5_input, c5_device):
+    # the stage bookkeeping check over every box of the 512 MiB round trip, in
+    # the default launch shape and in a deep ring with four groups in flight
+    for launch in (dict(checks=atb.CHECK_RING), dict(checks=atb.CHECK_RING, stages=6, store_groups=4)):
+        dst = dev_empty(w.storage_bytes, fill=0)
+        ms, md = encode(atb, w, c5_device), encode(atb, w, dst)
+        atb.tile_roundtrip(ms, md, **launch)
+        device_ok(atb)
+        assert_bytes_equal(host(dst), c5_input, f"{w.name} {launch}", view=oracle_view(w))
+
+
 @pytest.mark.parametrize("stages", [2, 4, 6, 8])
 @pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
 def test_c5_stage_sweep(atb, w, stages, c5_input, c5_device):
@@ -218,8 +230,10 @@ def _small_case(name, dtype, dims, box, swizzle, order, seed):
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 @pytest.mark.parametrize("launch", [dict(stages=1, ctas=1), dict(stages=3, ctas=5, store_groups=2),
                                     dict(stages=2, ctas=3, schedule="contiguous"), dict(),
-                                    dict(prefetch_boxes=3, l2_hints=3, poll_suspend_ns=20000)],
-                         ids=["s1c1", "s3c5g2", "s2c3contig", "default", "prefetch3_hints"])
+                                    dict(prefetch_boxes=3, l2_hints=3, poll_suspend_ns=20000),
+                                    dict(checks=1), dict(checks=1, stages=2, ctas=3, store_groups=2)],
+                         ids=["s1c1", "s3c5g2", "s2c3contig", "default", "prefetch3_hints", "ring_check",
+                              "ring_check_s2c3g2"])
 def test_small_cases_all_ops(atb, case, launch):
     name, dtype, dims, box, swizzle, order = case
     v, src_h, nbytes, coords_h = _small_case(name, dtype, dims, box, swizzle, order, 1000 + len(name))
@@ -394,8 +408,9 @@ def test_add_f32_day76_sixteen_tiles(atb):
 
 
 @pytest.mark.parametrize("swizzle,box", [("none", (64, 16)), ("128B", (32, 16)), ("64B", (16, 8))])
-@pytest.mark.parametrize("launch", [dict(), dict(stages=1, ctas=1), dict(stages=4, ctas=7, store_groups=3)],
-                         ids=["default", "s1c1", "s4c7g3"])
+@pytest.mark.parametrize("launch", [dict(), dict(stages=1, ctas=1), dict(stages=4, ctas=7, store_groups=3),
+                                    dict(checks=1, stages=3, ctas=5)],
+                         ids=["default", "s1c1", "s4c7g3", "ring_check"])
 def test_add_f32_ragged_lists_and_grid(atb, swizzle, box, launch):
     rows, cols = 300, 200
     strides = (4, 816)  # padded rows

@@ -51,6 +51,8 @@ def draw_case(seed):
         launch = dict(stages=int(g.integers(1, 7)), ctas=int(g.integers(1, 9)),
                       store_groups=int(g.integers(1, 4)), schedule=["strided", "contiguous"][g.integers(2)])
     n = int(g.integers(1, 90))
+    if seed % 2:  # every other case also runs the stage bookkeeping check (no draw, so cases stay put)
+        launch = dict(launch, checks=1)
     return dict(dtype=dtype, esize=esize, dims=tuple(dims), strides=tuple(strides), box=tuple(box),
                 swizzle=swizzle, steps=tuple(steps), nbytes=nbytes, launch=launch, n=n, seed=seed)
 
