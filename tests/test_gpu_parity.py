@@ -407,7 +407,8 @@ def test_add_f32_day76_sixteen_tiles(atb):
     assert_bytes_equal(host(dst), want, "day76 +1.0f", view=v)
 
 
-@pytest.mark.parametrize("swizzle,box", [("none", (64, 16)), ("128B", (32, 16)), ("64B", (16, 8))])
+@pytest.mark.parametrize("swizzle,box", [("none", (64, 16)), ("128B", (32, 16)), ("64B", (16, 8)),
+                                         ("none", (64, 128)), ("128B", (32, 160))])  # 32 KiB; 20 KiB boxes
 @pytest.mark.parametrize("launch", [dict(), dict(stages=1, ctas=1), dict(stages=4, ctas=7, store_groups=3),
                                     dict(checks=1, stages=3, ctas=5)],
                          ids=["default", "s1c1", "s4c7g3", "ring_check"])
