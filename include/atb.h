@@ -43,8 +43,11 @@
  *   - Errors raised inside a kernel (a wait that ran out of time, a misaligned
  *     box origin) are recorded in the device status block and reported by
  *     atb_device_status(); the kernel returns early instead of hanging.
- *   - Not thread-safe across host threads for atb_last_error(), which is
- *     thread-local; every other call may be used from any thread.
+ *   - Every call may be made from any host thread.  atb_last_error() is
+ *     kept per thread: it describes the last failed call of the calling
+ *     thread.  Host-resident round trips (atb_tile_roundtrip_host) share
+ *     one pair of transfer streams per device: concurrent calls are enqueued
+ *     one at a time and their copies run in that order.
  */
 #ifndef ATB_H
 #define ATB_H
