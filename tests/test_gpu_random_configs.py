@@ -67,7 +67,7 @@ def atb():
     return atb
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(400))
 def test_random_configuration(atb, seed):
     c = draw_case(10_000 + seed)
     v = oracle.View(c["esize"], c["dims"], c["strides"], c["box"], c["swizzle"], c["steps"])
