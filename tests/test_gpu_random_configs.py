@@ -67,9 +67,53 @@ def atb():
     return atb
 
 
+def draw_large_case(seed):
+    """Larger shapes: rank 2-3, boxes up to 256 along outer dimensions (at most
+    16 KiB per box), up to 2000 listed boxes, deeper rings, up to 39 CTAs, so
+    that every CTA wraps its ring many times and several store groups are in
+    flight."""
+    g = np.random.default_rng(seed)
+    dtype = DTYPES[g.integers(len(DTYPES))]
+    esize = datagen.ESIZE[dtype]
+    rank = int(g.integers(2, 4))
+    swizzle = ["none", "32B", "64B", "128B"][g.integers(4)]
+    box0 = (16 // esize) * int(g.integers(1, 17)) if swizzle == "none" else SPANS[swizzle] // esize
+    box0 = min(box0, 256)
+    budget = 16384 // (box0 * esize)
+    box, dims, steps = [box0], [int(g.integers(box0 // 2 + 1, 6 * box0 + 9))], [1]
+    for d in range(1, rank):
+        b = int(g.integers(1, max(2, min(256, budget) + 1)))
+        budget = max(1, budget // b)
+        box.append(b)
+        dims.append(int(g.integers(1, 5 * b + 3)))
+        steps.append(int([1, 1, 1, 2, 4][g.integers(5)]))
+    order = list(range(1, rank))
+    g.shuffle(order)
+    strides = [esize] + [0] * (rank - 1)
+    step = ((dims[0] * esize + 16 * int(g.integers(0, 3)) + 15) // 16) * 16
+    for d in order:
+        strides[d] = step
+        step *= dims[d]
+    launch = dict(stages=int(g.integers(1, 9)), ctas=int(g.integers(1, 40)), store_groups=int(g.integers(1, 5)),
+                  schedule=["strided", "contiguous"][g.integers(2)], checks=int(g.integers(2)))
+    if g.random() < 0.3:
+        launch = {}
+    return dict(dtype=dtype, esize=esize, dims=tuple(dims), strides=tuple(strides), box=tuple(box),
+                swizzle=swizzle, steps=tuple(steps), nbytes=max(step, 16), launch=launch,
+                n=int(g.integers(1, 2000)), seed=seed)
+
+
 @pytest.mark.parametrize("seed", range(400))
 def test_random_configuration(atb, seed):
-    c = draw_case(10_000 + seed)
+    _check_case(atb, draw_case(10_000 + seed))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_large_configuration(atb, seed):
+    _check_case(atb, draw_large_case(20_000 + seed), grid_round_trip=True)
+
+
+def _check_case(atb, c, grid_round_trip=False):
     v = oracle.View(c["esize"], c["dims"], c["strides"], c["box"], c["swizzle"], c["steps"])
     src_h = datagen.random_bytes(c["nbytes"], c["seed"])
     coords_h = datagen.random_box_origins(c["dims"], c["box"], c["esize"], c["n"], c["seed"] + 1)
@@ -117,6 +161,16 @@ def test_random_configuration(atb, seed):
     oracle.roundtrip(v, src_h, v, want2, coords_h)
     assert_bytes_equal(host(out2), want2, "listed round trip " + what)
 
+    if grid_round_trip:
+        out3 = dev_empty(c["nbytes"] + guard, fill=0x77)
+        md3 = atb.encode_tiled(c["dtype"], out3, c["dims"], c["strides"], c["box"], c["swizzle"],
+                               elem_strides=c["steps"])
+        atb.tile_roundtrip(ms, md3, None, 0, **c["launch"])
+        assert atb.device_status().code == 0
+        want3 = np.full(c["nbytes"] + guard, 0x77, dtype=np.uint8)
+        oracle.roundtrip(v, src_h, v, want3, grid_h)
+        assert_bytes_equal(host(out3), want3, "grid round trip " + what)
+
 
 def test_draws_cover_the_space():
     cases = [draw_case(10_000 + s) for s in range(40)]
@@ -124,3 +178,14 @@ def test_draws_cover_the_space():
     assert {len(c["dims"]) for c in cases} == {1, 2, 3, 4, 5}
     assert {c["swizzle"] for c in cases} == {"none", "32B", "64B", "128B"}
     assert any(max(c["steps"]) > 1 for c in cases)
+
+
+def test_large_draws_fit_and_vary():
+    cases = [draw_large_case(20_000 + s) for s in range(40)]
+    for c in cases:
+        bb = c["esize"]
+        for b, e in zip(c["box"], c["steps"]):
+            bb *= -(-b // e)
+        assert bb <= 16384 and all(1 <= b <= 256 for b in c["box"])
+    assert {c["swizzle"] for c in cases} == {"none", "32B", "64B", "128B"}
+    assert max(c["n"] for c in cases) > 1000 and any(c["launch"].get("checks") for c in cases)
