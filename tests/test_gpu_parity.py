@@ -332,6 +332,44 @@ def test_misaligned_origin_is_reported_and_skipped(atb):
     device_ok(atb)  # the report was reset by the previous read
 
 
+def test_origin_beyond_range_is_reported_and_never_issued(atb):
+    # origins beyond +-2^30 are refused per box before any copy is issued; the
+    # other boxes of the call still move
+    v = oracle.View(2, (128, 64), (2, 256), (64, 16))
+    src_h = datagen.random_bytes(64 * 256, 91)
+    src = dev_bytes(src_h)
+    far = (1 << 30) + 16
+    coords_h = np.array([[0, 0], [0, far], [64, 16], [-far, 0], [64, 48]], dtype=np.int32)
+    coords = dev_bytes(coords_h.view(np.uint8))
+    good = [0, 2, 4]
+    ms = atb.encode_tiled("f16", src, v.dims, v.strides, v.box)
+    bb = atb.box_bytes(ms)
+
+    packed = dev_empty(5 * bb, fill=0xEE)
+    atb.tile_load(ms, coords, 5, packed, stages=2, ctas=1)
+    rep = atb.device_status()
+    assert rep.code == atb.ATB_ERR_COORD_RANGE and rep.tile == 1 and rep.errors == 2, rep.as_dict()
+    got = host(packed).reshape(5, bb)
+    want = oracle.tile_load(v, src_h, coords_h[good]).reshape(3, bb)
+    for i, j in enumerate(good):
+        assert_bytes_equal(got[j], want[i], f"box {j}")
+    assert (got[[1, 3]] == 0xEE).all()  # refused boxes left untouched
+
+    for op in ("store", "roundtrip"):
+        out = dev_empty(64 * 256, fill=0x5A)
+        md = atb.encode_tiled("f16", out, v.dims, v.strides, v.box)
+        if op == "store":
+            atb.tile_store(md, coords, 5, packed)
+        else:
+            atb.tile_roundtrip(ms, md, coords, 5)
+        rep = atb.device_status()
+        assert rep.code == atb.ATB_ERR_COORD_RANGE and rep.errors == 2, (op, rep.as_dict())
+        want_t = np.full(64 * 256, 0x5A, dtype=np.uint8)
+        oracle.tile_store(v, want_t, coords_h[good], oracle.tile_load(v, src_h, coords_h[good]))
+        assert_bytes_equal(host(out), want_t, f"{op} with refused origins")
+    device_ok(atb)
+
+
 def test_bounded_wait_times_out_and_gpu_stays_usable(atb):
     import time
 
