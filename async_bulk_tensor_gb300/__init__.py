@@ -154,6 +154,67 @@ def _ptr(x) -> int | None:
     raise TypeError(f"expected a pointer (int) or an object with data_ptr(), got {type(x).__name__}")
 
 
+ESIZE = {"u8": 1, "u16": 2, "u32": 4, "i32": 4, "u64": 8, "i64": 8, "f16": 2, "f32": 4, "f64": 8, "bf16": 2}
+
+
+def _bytes_from(x) -> int | None:
+    """Bytes a torch tensor can reach from its data pointer to the end of its
+    storage, or a numpy array's size; None for a raw pointer."""
+    if hasattr(x, "untyped_storage"):
+        return int(x.untyped_storage().nbytes()) - int(x.storage_offset()) * int(x.element_size())
+    if hasattr(x, "nbytes") and hasattr(x, "ctypes"):
+        return int(x.nbytes)
+    return None
+
+
+def _device_ptr(x, need: int, what: str) -> int | None:
+    """Device address of ``x`` for a call that touches ``need`` bytes from it.
+
+    A torch tensor must live on a CUDA device and reach at least ``need`` bytes
+    from its data pointer; anything else raises AtbError(ATB_ERR_ARG) before the
+    library is called, so that a host buffer or a short one never reaches a
+    kernel.  Raw integer addresses are passed through unchecked, as in C.
+    """
+    if x is None or isinstance(x, int):
+        return x
+    if getattr(x, "is_cuda", None) is False or (hasattr(x, "ctypes") and hasattr(x, "dtype")):
+        raise AtbError(ATB_ERR_ARG, what, f"{what} is in host memory; this call needs device memory")  # noqa: F821
+    have = _bytes_from(x)
+    if have is not None and have < need:
+        raise AtbError(ATB_ERR_ARG, what, f"{what} reaches {have} bytes; the call touches {need}")  # noqa: F821
+    return _ptr(x)
+
+
+def _host_ptr(x, need: int, what: str) -> int:
+    """Host address of ``x`` (a CPU tensor, a numpy array or an int) for a call
+    that touches ``need`` bytes from it; a device tensor or a short buffer
+    raises AtbError(ATB_ERR_ARG)."""
+    if isinstance(x, int):
+        return x
+    if getattr(x, "is_cuda", False):
+        raise AtbError(ATB_ERR_ARG, what, f"{what} is device memory; this call needs host memory")  # noqa: F821
+    have = _bytes_from(x)
+    if have is not None and have < need:
+        raise AtbError(ATB_ERR_ARG, what, f"{what} reaches {have} bytes; the call touches {need}")  # noqa: F821
+    return x.ctypes.data if hasattr(x, "ctypes") and hasattr(x, "dtype") else _ptr(x)
+
+
+def span_bytes(m: "TensorMap") -> int:
+    """Bytes from a map's base to one past its last element."""
+    span = int(m.esize)
+    for d in range(int(m.rank)):
+        span += (int(m.dims[d]) - 1) * (int(m.esize) if d == 0 else int(m.strides[d]))
+    return span
+
+
+def _boxes(m: "TensorMap", coords, n: int) -> int:
+    return int(n) if coords is not None else grid_tiles(m)
+
+
+def _coords_ptr(m: "TensorMap", coords, n: int) -> int | None:
+    return _device_ptr(coords, int(n) * int(m.rank) * 4, "coordinate list")
+
+
 def _stream(s) -> int | None:
     if s is None:
         torch = sys.modules.get("torch")
@@ -195,6 +256,11 @@ def encode_tiled(dtype: str, base, dims, strides_bytes, box, swizzle="none", l2_
     ``oob_fill`` is "zero" or "nan" (floating-point types only).
     """
     rank = len(dims)
+    if not isinstance(base, int) and base is not None and isinstance(dtype, str) and dtype in ESIZE \
+            and strides_bytes is not None and len(strides_bytes) == rank and rank >= 1:
+        need = ESIZE[dtype] + sum((int(dims[d]) - 1) * (ESIZE[dtype] if d == 0 else int(strides_bytes[d]))
+                                  for d in range(rank))
+        _device_ptr(base, need, "tensor base")
     m = TensorMap()
     a_dims = (ctypes.c_uint64 * max(rank, 1))(*[int(d) for d in dims])
     a_str = (ctypes.c_uint64 * max(rank, 1))(*[int(s) for s in strides_bytes]) if strides_bytes is not None else None
@@ -225,19 +291,23 @@ def pipeline_smem_bytes(m: TensorMap, stages: int) -> int:
 
 def tile_load(src: TensorMap, coords, n: int, packed, stream=None, **launch):
     """``atb_tile_load``: gather boxes into packed images; ``coords=None`` = tile grid."""
-    _check(lib.atb_tile_load(ctypes.byref(src), _ptr(coords), int(n), _ptr(packed),
-                             ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_load")
+    c = _coords_ptr(src, coords, n)
+    p = _device_ptr(packed, _boxes(src, coords, n) * box_bytes(src), "packed buffer")
+    _check(lib.atb_tile_load(ctypes.byref(src), c, int(n), p, ctypes.byref(_launch(**launch)), _stream(stream)),
+           "atb_tile_load")
 
 
 def tile_store(dst: TensorMap, coords, n: int, packed, stream=None, **launch):
     """``atb_tile_store``: scatter packed images into the tensor; ``coords=None`` = tile grid."""
-    _check(lib.atb_tile_store(ctypes.byref(dst), _ptr(coords), int(n), _ptr(packed),
-                              ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_store")
+    c = _coords_ptr(dst, coords, n)
+    p = _device_ptr(packed, _boxes(dst, coords, n) * box_bytes(dst), "packed buffer")
+    _check(lib.atb_tile_store(ctypes.byref(dst), c, int(n), p, ctypes.byref(_launch(**launch)), _stream(stream)),
+           "atb_tile_store")
 
 
 def tile_roundtrip(src: TensorMap, dst: TensorMap, coords=None, n: int = 0, stream=None, **launch):
     """``atb_tile_roundtrip``: store(dst, coords, load(src, coords)); ``coords=None`` = tile grid."""
-    _check(lib.atb_tile_roundtrip(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
+    _check(lib.atb_tile_roundtrip(ctypes.byref(src), ctypes.byref(dst), _coords_ptr(src, coords, n), int(n),
                                   ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_roundtrip")
 
 
@@ -247,17 +317,16 @@ def tile_roundtrip_host(src: TensorMap, dst: TensorMap, h_src, h_dst, slabs: int
     ``h_src``/``h_dst`` are host pointers (ints, or CPU tensors / numpy arrays
     via ``data_ptr()``/``ctypes.data``), laid out as the device maps describe.
     """
-    def hptr(x):
-        return x.ctypes.data if hasattr(x, "ctypes") and hasattr(x, "dtype") else _ptr(x)
-
-    _check(lib.atb_tile_roundtrip_host(ctypes.byref(src), ctypes.byref(dst), hptr(h_src), hptr(h_dst), int(slabs),
+    hs = _host_ptr(h_src, span_bytes(src), "host source")
+    hd = _host_ptr(h_dst, span_bytes(dst), "host destination")
+    _check(lib.atb_tile_roundtrip_host(ctypes.byref(src), ctypes.byref(dst), hs, hd, int(slabs),
                                        ctypes.byref(_launch(**launch)), _stream(stream)), "atb_tile_roundtrip_host")
 
 
 def tile_roundtrip_add_f32(src: TensorMap, dst: TensorMap, addend: float, coords=None, n: int = 0, stream=None,
                            **launch):
     """``atb_tile_roundtrip_add_f32``: store(dst, coords, load(src, coords) + addend) in fp32."""
-    _check(lib.atb_tile_roundtrip_add_f32(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
+    _check(lib.atb_tile_roundtrip_add_f32(ctypes.byref(src), ctypes.byref(dst), _coords_ptr(src, coords, n), int(n),
                                           float(addend), ctypes.byref(_launch(**launch)), _stream(stream)),
            "atb_tile_roundtrip_add_f32")
 
@@ -271,7 +340,7 @@ def tile_roundtrip_noalloc(src: TensorMap, dst: TensorMap, coords=None, n: int =
     it returns None right after the launch.
     """
     rep = DeviceReport() if report else None
-    code = lib.atb_tile_roundtrip_noalloc(ctypes.byref(src), ctypes.byref(dst), _ptr(coords), int(n),
+    code = lib.atb_tile_roundtrip_noalloc(ctypes.byref(src), ctypes.byref(dst), _coords_ptr(src, coords, n), int(n),
                                           ctypes.byref(_launch(**launch)), _stream(stream),
                                           ctypes.byref(rep) if rep is not None else None)
     if rep is None or code != rep.code:
@@ -308,14 +377,17 @@ def selftest_wait_timeout(timeout_ns: int, stream=None):
 
 
 def copy_cpasync(src, dst, nbytes: int, stream=None, **launch):
-    _check(lib.atb_copy_cpasync(_ptr(src), _ptr(dst), int(nbytes), ctypes.byref(_launch(**launch)),
+    _check(lib.atb_copy_cpasync(_device_ptr(src, int(nbytes), "source"), _device_ptr(dst, int(nbytes), "destination"),
+                                int(nbytes), ctypes.byref(_launch(**launch)),
                                 _stream(stream)), "atb_copy_cpasync")
 
 
 def copy_ldst_v4(src, dst, nbytes: int, stream=None, **launch):
-    _check(lib.atb_copy_ldst_v4(_ptr(src), _ptr(dst), int(nbytes), ctypes.byref(_launch(**launch)),
+    _check(lib.atb_copy_ldst_v4(_device_ptr(src, int(nbytes), "source"), _device_ptr(dst, int(nbytes), "destination"),
+                                int(nbytes), ctypes.byref(_launch(**launch)),
                                 _stream(stream)), "atb_copy_ldst_v4")
 
 
 def copy_memcpy(src, dst, nbytes: int, stream=None):
-    _check(lib.atb_copy_memcpy(_ptr(src), _ptr(dst), int(nbytes), _stream(stream)), "atb_copy_memcpy")
+    _check(lib.atb_copy_memcpy(_device_ptr(src, int(nbytes), "source"), _device_ptr(dst, int(nbytes), "destination"),
+                               int(nbytes), _stream(stream)), "atb_copy_memcpy")

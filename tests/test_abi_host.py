@@ -122,3 +122,64 @@ def test_unknown_check_bits_are_rejected_before_any_device_work(atb):
     with pytest.raises(atb.AtbError) as e:
         atb.tile_roundtrip(m, m, checks=2)
     assert e.value.code == atb.ATB_ERR_ARG and "check bits" in str(e.value)
+
+
+class _FakeDeviceTensor:
+    """Just enough of a CUDA tensor for the binding's buffer checks (no GPU)."""
+
+    is_cuda = True
+
+    def __init__(self, nbytes, offset=0):
+        self._n, self._off = nbytes, offset
+
+    def untyped_storage(self):
+        n = self._n
+
+        class _S:
+            def nbytes(self):
+                return n
+
+        return _S()
+
+    def storage_offset(self):
+        return self._off
+
+    def element_size(self):
+        return 1
+
+    def data_ptr(self):
+        return 0x10000 + self._off
+
+
+def test_binding_refuses_host_and_short_buffers_before_the_library(atb):
+    import numpy as np
+    import torch
+
+    m = atb.TensorMap()
+    m.magic, m.rank, m.esize, m.dtype = 0x31425441, 2, 2, atb.DTYPES["f16"]
+    m.base, m.box_bytes = 0x10000, 2048
+    for d, (n, b) in enumerate(((1024, 64), (64, 16))):
+        m.dims[d], m.box[d], m.elem_strides[d] = n, b, 1
+    m.strides[0], m.strides[1] = 2, 2048
+    assert atb.span_bytes(m) == 63 * 2048 + 1024 * 2
+    cases = [
+        (lambda: atb.tile_load(m, None, 0, torch.empty(1 << 20, dtype=torch.uint8)), "host memory"),
+        (lambda: atb.tile_load(m, None, 0, np.empty(1 << 20, dtype=np.uint8)), "host memory"),
+        (lambda: atb.tile_load(m, None, 0, _FakeDeviceTensor(64 * 2048 - 1)), "touches 131072"),  # 64 boxes
+        (lambda: atb.tile_store(m, _FakeDeviceTensor(8 * 2 * 4 - 4), 8, _FakeDeviceTensor(1 << 20)), "coordinate"),
+        (lambda: atb.tile_store(m, _FakeDeviceTensor(64), 8, _FakeDeviceTensor(8 * 2048 - 16, 16)), "packed"),
+        (lambda: atb.tile_roundtrip(m, m, torch.zeros(16, dtype=torch.int32), 8), "host memory"),
+        (lambda: atb.tile_roundtrip_host(m, m, np.empty(atb.span_bytes(m) - 1, np.uint8),
+                                         np.empty(atb.span_bytes(m), np.uint8)), "host source"),
+        (lambda: atb.tile_roundtrip_host(m, m, np.empty(atb.span_bytes(m), np.uint8),
+                                         _FakeDeviceTensor(1 << 20)), "device memory"),
+        (lambda: atb.encode_tiled("f16", torch.empty(4096, dtype=torch.uint8), (1024, 64), (2, 2048), (64, 16)),
+         "host memory"),
+        (lambda: atb.encode_tiled("f16", _FakeDeviceTensor(atb.span_bytes(m) - 2), (1024, 64), (2, 2048), (64, 16)),
+         "tensor base"),
+        (lambda: atb.copy_memcpy(_FakeDeviceTensor(100), _FakeDeviceTensor(99), 100), "destination"),
+    ]
+    for call, text in cases:
+        with pytest.raises(atb.AtbError) as e:
+            call()
+        assert e.value.code == atb.ATB_ERR_ARG and text in str(e.value), str(e.value)

@@ -396,10 +396,21 @@ def test_host_side_errors(atb):
     with pytest.raises(atb.AtbError) as e:
         atb.tile_load(ms, None, 0, b, stages=17)
     assert e.value.code == atb.ATB_ERR_ARG
-    big = atb.encode_tiled("f16", a, (256, 256), (2, 512), (256, 256))
+    c = dev_empty(1 << 17)
+    big = atb.encode_tiled("f16", c, (256, 256), (2, 512), (256, 256))
     with pytest.raises(atb.AtbError) as e:
         atb.tile_roundtrip(big, big, stages=2)
     assert e.value.code == atb.ATB_ERR_SMEM_BUDGET
+    # the binding refuses buffers a call would overrun, and host memory, before the library runs
+    with pytest.raises(atb.AtbError) as e:
+        atb.encode_tiled("f16", a, (256, 256), (2, 512), (256, 256))
+    assert e.value.code == atb.ATB_ERR_ARG and "tensor base" in str(e.value)
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_load(ms, None, 0, b[: atb.grid_tiles(ms) * atb.box_bytes(ms) - 1].clone())
+    assert e.value.code == atb.ATB_ERR_ARG and "packed buffer" in str(e.value)
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_load(ms, None, 0, b.cpu())
+    assert e.value.code == atb.ATB_ERR_ARG and "host memory" in str(e.value)
     device_ok(atb)
 
 
