@@ -265,9 +265,10 @@ def test_small_cases_all_ops(atb, case, launch):
     assert_bytes_equal(got_g, oracle.tile_load(v, src_h, grid_h), f"{name} grid load", image_bytes=bb)
     assert (got_g[len(grid_h) * bb:] == 0xEE).all(), f"{name} grid load wrote past the packed buffer"
 
-    # scatter of random images to listed origins (later boxes overwrite earlier
-    # ones where they overlap, so use disjoint-content-free check: one box per
-    # call sequence is order-free only without overlap -> use the grid here)
+    # scatter of random images: over the tile grid, whose boxes are disjoint, so
+    # the result does not depend on the order the boxes are written in (listed
+    # origins may overlap; they are stored below with images of one load, which
+    # carry identical bytes wherever boxes overlap)
     images_h = datagen.random_bytes(len(grid_h) * bb, 7)
     images = dev_bytes(images_h)
     out = dev_empty(nbytes + guard, fill=0x5A)  # bytes past the tensor must stay 0x5A
