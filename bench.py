@@ -15,8 +15,10 @@ Prints ONE JSON line (rank 0):
   e2e        the same metric through the public call with HOST buffers:
              pinned H2D of the input, encode, round trip, D2H of the output
   roofline   the round-trip kernel against the measured copy bandwidth
-  cpu_baseline  the plain CPU oracle on the host cores (single thread)
+  cpu_baseline  the plain CPU oracle on one host core, and (all_cores) the
+             same round trip split over every host core
   sweep / ablations  stage sweep and the thread-issued copies beside it
+  workloads  the smaller workloads, L2-warm and after an L2 flush
 
 ``--impl reference`` times the oracle instead (the reference arm).
 Inputs (512 MiB in + 512 MiB out) exceed the 129 MB L2, so no flush is needed.
