@@ -85,6 +85,10 @@ struct Control {
     // consumer last released it from, modulo 256); 0 = not used yet.
     uint32_t filled[kMaxStages];
     uint32_t freed[kMaxStages];
+    // Listed boxes: the origin of the box each stage holds, written by the
+    // producer before it arms the stage, so that consumers never read the
+    // coordinate list in global memory.
+    int32_t origin[kMaxStages][ATB_MAX_RANK];
 };
 
 __device__ __forceinline__ void record_error(DeviceStatus* st, int32_t code, int32_t tile, int32_t where)
@@ -441,6 +445,22 @@ __device__ __forceinline__ void ring_check_filled(const PipeArgs& a, const Ring&
         record_error(a.status, ATB_ERR_RING_CHECK, static_cast<int32_t>(tile), kWhereConsumerRing);
 }
 
+// Origin of the box that landed in stage s: from the cursor for the tile grid,
+// from the stage's origin slot for listed boxes.  Read after the stage's
+// full-barrier wait, which orders it after the producer's write.
+template <int R>
+__device__ __forceinline__ void landed_origin(const PipeArgs& a, const Ring& r, uint32_t s, const BoxCursor<R>& cur,
+                                              int32_t (&c)[R])
+{
+    if (a.coords) {
+        const volatile int32_t* slot = r.ctl->origin[s];
+#pragma unroll
+        for (int d = 0; d < R; ++d) c[d] = slot[d];
+    } else {
+        cur.origin(a, c);
+    }
+}
+
 // One producer thread: for its k-th box, wait until stage k mod N is free,
 // arm the stage's full barrier with the box's byte count and issue the copy.
 template <int MODE, int R>
@@ -465,6 +485,10 @@ __device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, con
             tile_origin<R>(a, tile_of(a, k + a.prefetch), c);
             if (!origin_error<R>(a, c)) ptx::tma_prefetch_l2<R>(&src_map, c);
         }
+        // The origin first: for listed boxes it is a load from the coordinate
+        // list, whose latency then overlaps the wait for the stage.
+        int32_t c[R];
+        cur.origin(a, c);
         // the stage's previous use completed the empty phase of the other parity
         if (k >= S && !wait_bounded(r.empty(s), cur.parity ^ 1u, a.timeout_ns, r.abort_flag(), a.suspend_ns)) {
             raise_abort(a, r, cur.t, kWhereProducerWait);
@@ -474,8 +498,11 @@ __device__ void producer_loop(const PipeArgs& a, const CUtensorMap& src_map, con
         ring_check_freed(a, r, s, k, t);
         if (a.checks & ATB_CHECK_RING)  // published by the arrive below (release order)
             *reinterpret_cast<volatile uint32_t*>(&r.ctl->filled[s]) = k + 1u;
-        int32_t c[R];
-        cur.origin(a, c);
+        if (a.coords) {  // hand the origin over with the stage (published by the arrive below)
+            volatile int32_t* slot = r.ctl->origin[s];
+#pragma unroll
+            for (int d = 0; d < R; ++d) slot[d] = c[d];
+        }
         const int32_t bad = origin_error<R>(a, c);
         if (bad) {
             record_error(a.status, bad, static_cast<int32_t>(t), kWhereProducerIssue);
@@ -594,7 +621,12 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
         const uint32_t t = cur.t;
         if (lane == 0) ring_check_filled(a, r, s, k, t);
         int32_t c[R];
-        cur.origin(a, c);
+        // Lane 0 reads the slot and the warp takes its copy: a lane that ran
+        // late could otherwise read the slot after lane 0 has freed the stage
+        // and the producer has refilled it.
+        if (lane == 0) landed_origin<R>(a, r, s, cur, c);
+#pragma unroll
+        for (int d = 0; d < R; ++d) c[d] = __shfl_sync(0xffffffffu, c[d], 0);
         const bool skip = origin_error<R>(a, c) != 0;
         // kLoad: kStoreTensor means "drain the image to the packed buffer"
         const int kind = skip ? kStoreNothing : (MODE == kLoad ? kStoreTensor : store_kind<R>(a, c));
@@ -683,8 +715,10 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
             break;
         }
         if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
+        // Every consumer thread reads the slot here, before the barrier that
+        // precedes any release of the stage.
         int32_t c[R];
-        cur.origin(a, c);
+        landed_origin<R>(a, r, s, cur, c);
         const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
         if (ADD && kind != kStoreNothing) {
             // generic-proxy update of the landed box; element order is irrelevant.
