@@ -620,13 +620,20 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
         }
         const uint32_t t = cur.t;
         if (lane == 0) ring_check_filled(a, r, s, k, t);
-        int32_t c[R];
-        // Lane 0 reads the slot and the warp takes its copy: a lane that ran
-        // late could otherwise read the slot after lane 0 has freed the stage
-        // and the producer has refilled it.
-        if (lane == 0) landed_origin<R>(a, r, s, cur, c);
+        int32_t c[R] = {};
+        if (!a.coords) {
+            cur.origin(a, c);  // the tile grid: every lane follows the same cursor
+        } else if (MODE == kLoad) {
+            // a gathered box is drained by lane 0 alone; no other lane needs it
+            if (lane == 0) landed_origin<R>(a, r, s, cur, c);
+        } else {
+            // Lane 0 reads the slot and the warp takes its copy: a lane that
+            // ran late could otherwise read the slot after lane 0 has freed
+            // the stage and the producer has refilled it.
+            if (lane == 0) landed_origin<R>(a, r, s, cur, c);
 #pragma unroll
-        for (int d = 0; d < R; ++d) c[d] = __shfl_sync(0xffffffffu, c[d], 0);
+            for (int d = 0; d < R; ++d) c[d] = __shfl_sync(0xffffffffu, c[d], 0);
+        }
         const bool skip = origin_error<R>(a, c) != 0;
         // kLoad: kStoreTensor means "drain the image to the packed buffer"
         const int kind = skip ? kStoreNothing : (MODE == kLoad ? kStoreTensor : store_kind<R>(a, c));
