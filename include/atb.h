@@ -283,10 +283,14 @@ atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, s
  *   src       encoded map of the source tensor
  *   d_coords  device array of n * rank int32 origins, innermost first; NULL =
  *             every box of the tile grid in row-major tile order (innermost
- *             tile index fastest), n is then ignored
+ *             tile index fastest), n is then ignored.  The producer thread
+ *             reads each origin once and hands it to the consumers with the
+ *             stage.
  *   d_packed  device output, 16-byte aligned, n * box_bytes bytes
  *   launch    NULL for defaults
- * n = 0 launches nothing.
+ * n = 0 launches nothing.  The kernel reads d_coords and the source, and
+ * writes d_packed, while it runs on `stream`: the caller keeps them allocated
+ * and unchanged (d_packed unread) until the stream has passed the call.
  */
 atb_status atb_tile_load(const atb_tensor_map* src, const int32_t* d_coords, uint64_t n,
                          void* d_packed, const atb_launch* launch, atb_stream_t stream);
