@@ -11,8 +11,9 @@ namespace atb {
 constexpr uint32_t kMapMagic = 0x31425441u;  // "ATB1"
 constexpr uint32_t kMaxStages = 16;
 constexpr uint32_t kPipelineThreads = 64;    // warp 0 producer, warp 1 consumer
-constexpr uint32_t kConsumerThreads = 128;   // transform kernel: warps 1..4 update the stage
+constexpr uint32_t kConsumerThreads = 128;   // wide kernel, listed stores: warps 1..4 share clipped stores
 constexpr uint32_t kTransformThreads = 32 + kConsumerThreads;
+constexpr uint32_t kUpdateConsumerThreads = 64;  // wide kernel, fp32 update: warps 1..2 update the stage
 constexpr uint32_t kStageAlignSwizzled = 1024;  // one period of the 128-byte swizzle
 constexpr uint32_t kStageAlignPlain = 128;
 

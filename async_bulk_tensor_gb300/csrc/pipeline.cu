@@ -667,20 +667,21 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
     if (failed) drain_after_failure(a, r, k);
 }
 
-// The pipeline with four consumer warps: warp 0 lane 0 produces, warps 1..4
-// share each landed stage, and consumer thread 0 issues the tensor store.
+// The pipeline with several consumer warps: warp 0 lane 0 produces, the
+// consumer warps share each landed stage, and consumer thread 0 issues the
+// tensor store.
 //   ADD   round trip with an elementwise fp32 update in shared memory between
 //         the load and the store ("Day 76: The Tensor Memory Accelerator
 //         (TMA)", "Exercise" and "Solution": the threads change the tile in
 //         shared memory, every writer publishes its writes across the proxy
 //         line with fence.proxy.async, the group meets at a barrier, and one
 //         thread issues the tensor store).  Each element becomes x + addend in
-//         round-to-nearest fp32.
+//         round-to-nearest fp32.  Two consumer warps.
 //   !ADD  a plain round trip or store whose boxes come from a list, where
-//         boxes that start before the tensor are common: 128 threads share
-//         the clipped stores of such boxes instead of one warp.
+//         boxes that start before the tensor are common: four consumer warps
+//         share the clipped stores of such boxes instead of one warp.
 template <int MODE, int R, bool ADD>
-__global__ void __launch_bounds__(kTransformThreads, 1)
+__global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumerThreads), 1)
     tile_wide_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
                      const PipeArgs a, float addend)
 {
@@ -703,7 +704,9 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
         return;
     }
 
-    const uint32_t ct = threadIdx.x - 32;  // consumer thread 0 .. kConsumerThreads-1
+    // consumer threads: fewer for the update (measured faster), more for clipped stores
+    constexpr uint32_t CT = ADD ? kUpdateConsumerThreads : kConsumerThreads;
+    const uint32_t ct = threadIdx.x - 32;  // consumer thread 0 .. CT-1
     const uint32_t chunks = a.box_bytes / 16;
     PendingStores pending;  // consumer thread 0's store groups still reading their stages
     BoxCursor<R> cur;
@@ -717,7 +720,7 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
             failed = true;
         }
         // every consumer warp must agree before any of them leaves the loop
-        if (ptx::named_barrier_or(1, kConsumerThreads, failed)) {
+        if (ptx::named_barrier_or(1, CT, failed)) {
             failed = true;
             break;
         }
@@ -734,19 +737,19 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
             // shared-memory latency is paid per pass instead of one per chunk.
             const uint32_t base = r.stage(s);
             uint32_t j = ct;
-            for (; j + 7 * kConsumerThreads < chunks; j += 8 * kConsumerThreads) {
+            for (; j + 7 * CT < chunks; j += 8 * CT) {
                 float v[8][4];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ptx::ld_shared_v4_f32(base + 16 * (j + u * kConsumerThreads), v[u]);
+                for (int u = 0; u < 8; ++u) ptx::ld_shared_v4_f32(base + 16 * (j + u * CT), v[u]);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) v[u][e] = __fadd_rn(v[u][e], addend);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ptx::st_shared_v4_f32(base + 16 * (j + u * kConsumerThreads), v[u]);
+                for (int u = 0; u < 8; ++u) ptx::st_shared_v4_f32(base + 16 * (j + u * CT), v[u]);
             }
-            for (; j < chunks; j += kConsumerThreads) {  // the rest of a box that is not a multiple of 16 KiB
+            for (; j < chunks; j += CT) {  // the rest of a box that is not a multiple of 8 x 16 x CT bytes
                 float v[4];
                 ptx::ld_shared_v4_f32(base + 16 * j, v);
 #pragma unroll
@@ -755,10 +758,10 @@ __global__ void __launch_bounds__(kTransformThreads, 1)
             }
             ptx::fence_proxy_async_smem();  // each writer publishes its own writes to the async proxy
         }
-        ptx::named_barrier_sync(1, kConsumerThreads);
+        ptx::named_barrier_sync(1, CT);
         if (kind == kStorePlain) {
-            plain_store_box<R>(a, c, r.stage(s), ct, kConsumerThreads);
-            ptx::named_barrier_sync(1, kConsumerThreads);  // every reader is done with the stage
+            plain_store_box<R>(a, c, r.stage(s), ct, CT);
+            ptx::named_barrier_sync(1, CT);  // every reader is done with the stage
         }
         if (ct == 0) {
             if (kind == kStoreTensor) {
@@ -941,7 +944,9 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     if (MODE == kRoundtripAddF32) wide_fn = wide_kernel_for_rank<kRoundtrip, true>(rank);
     else if (wide) wide_fn = wide_kernel_for_rank<kBase == kLoad ? kRoundtrip : kBase, false>(rank);
     const void* fn = wide ? reinterpret_cast<const void*>(wide_fn) : reinterpret_cast<const void*>(kernel_for_rank<kBase>(rank));
-    const uint32_t threads = wide ? kTransformThreads : kPipelineThreads;
+    const uint32_t threads = MODE == kRoundtripAddF32 ? 32 + kUpdateConsumerThreads
+                             : wide                     ? kTransformThreads
+                                                        : kPipelineThreads;
     st = prepare_kernel(fn, dev);
     if (st != ATB_OK) return st;
 
