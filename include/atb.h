@@ -378,7 +378,7 @@ atb_status atb_tile_roundtrip_host(const atb_tensor_map* src, const atb_tensor_m
  * the tile in shared memory through the generic proxy, each writer then
  * publishes its writes with fence.proxy.async, the group meets at a barrier
  * and one thread issues the tensor store, completed through a bulk async
- * group.  Four consumer warps update each stage; one producer thread loads.
+ * group.  Two consumer warps update each stage; one producer thread loads.
  *
  *   src, dst  ATB_F32 maps with equal rank, box extents and swizzle
  *             (ATB_ERR_DTYPE / ATB_ERR_ARG otherwise)
