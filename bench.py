@@ -488,12 +488,11 @@ def end_to_end(torch, atb, w, device, stream, src_h, nbytes, bytes_per_step, arg
     steps = max(3, args.e2e_steps)
     seconds = time_launches(torch, stream, step, steps, 3, dist, device)
     atb.check_device(stream)
-    ok = bool((out_pin[:1 << 20] == src_pin[:1 << 20]).all()) and bool(torch.equal(out_pin[-(1 << 20):],
-                                                                                      src_pin[-(1 << 20):]))
+    ok = bool(torch.equal(out_pin, src_pin))  # the whole host output of the last step
     units, max_s = aggregate(dist, seconds, float(bytes_per_step) * steps, device)
     return {"value": round(units / max_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": nbytes, "steps": steps, "ms_per_step": round(max_s / steps * 1e3, 3),
-            "slabs": args.slabs or 12, "call": "atb_tile_roundtrip_host", "verified_sample": ok}
+            "slabs": args.slabs or 12, "call": "atb_tile_roundtrip_host", "verified": ok}
 
 
 def cpu_baseline(w, src_h, repeats: int = 4):
@@ -602,7 +601,7 @@ def main(argv=None):
     p.add_argument("--stages", type=int, default=0, help="0 = library default")
     p.add_argument("--ctas-per-sm", type=int, default=0, help="0 = library default")
     p.add_argument("--poll-suspend-ns", type=int, default=0, help="mbarrier poll suspend hint (0 = default)")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--slabs", type=int, default=0, help="host round trip slabs (0 = library default)")
     p.add_argument("--ref-tiles", type=int, default=0,
                    help="boxes per reference-arm step (0 = sized from --steps/--warmup)")
