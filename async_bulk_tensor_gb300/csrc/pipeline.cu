@@ -719,16 +719,17 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
         if (!__all_sync(0xffffffffu, ok)) {
             failed = true;
         }
+        // Every consumer thread reads the origin slot before the barrier
+        // below; consumer thread 0 frees the stage only after that barrier, so
+        // no thread can see the slot refilled for a later box.
+        int32_t c[R];
+        landed_origin<R>(a, r, s, cur, c);
         // every consumer warp must agree before any of them leaves the loop
         if (ptx::named_barrier_or(1, CT, failed)) {
             failed = true;
             break;
         }
         if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
-        // Every consumer thread reads the slot here, before the barrier that
-        // precedes any release of the stage.
-        int32_t c[R];
-        landed_origin<R>(a, r, s, cur, c);
         const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
         if (ADD && kind != kStoreNothing) {
             // generic-proxy update of the landed box; element order is irrelevant.
@@ -758,7 +759,7 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
             }
             ptx::fence_proxy_async_smem();  // each writer publishes its own writes to the async proxy
         }
-        ptx::named_barrier_sync(1, CT);
+        if (ADD) ptx::named_barrier_sync(1, CT);  // the update is complete and fenced before any store
         if (kind == kStorePlain) {
             plain_store_box<R>(a, c, r.stage(s), ct, CT);
             ptx::named_barrier_sync(1, CT);  // every reader is done with the stage
