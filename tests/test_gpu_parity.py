@@ -919,3 +919,44 @@ def test_independent_calls_on_four_streams(atb):
     want_u = np.zeros(w4.storage_bytes, dtype=np.uint8)
     oracle.roundtrip_add_f32(v4, s4_h, v4, want_u, oracle.grid_coords(v4), -2.5)
     assert_bytes_equal(host(upd), want_u, "stream 4 fp32 update")
+
+
+# --------------------------------------------------------------------------
+# round trips between different views: the maps share box, element size and
+# swizzle, while extents, strides and dimension order differ
+# --------------------------------------------------------------------------
+VIEW_PAIRS = [
+    # name, dtype, src dims, dst dims, box, swizzle, src outer order, dst outer order
+    ("f16_into_smaller", "f16", (300, 77), (200, 50), (64, 16), "none", None, None),
+    ("bf16_into_larger_sw128", "bf16", (130, 40), (260, 90), (64, 8), "128B", None, None),
+    ("f32_3d_permuted_dst", "f32", (64, 20, 7), (40, 9, 11), (16, 8, 3), "64B", None, [2, 1]),
+    ("u8_ragged_rows", "u8", (333, 41), (201, 29), (32, 8), "32B", None, None),
+]
+
+
+@pytest.mark.parametrize("case", VIEW_PAIRS, ids=[c[0] for c in VIEW_PAIRS])
+@pytest.mark.parametrize("listed", [False, True], ids=["grid", "listed"])
+def test_round_trip_between_different_views(atb, case, listed):
+    name, dtype, sdims, ddims, box, swizzle, sorder, dorder = case
+    esize = datagen.ESIZE[dtype]
+    sstr, sbytes = _strides(esize, sdims, order=sorder)
+    dstr, dbytes = _strides(esize, ddims, pitch_pad=48, order=dorder)
+    vs = oracle.View(esize, sdims, sstr, box, swizzle)
+    vd = oracle.View(esize, ddims, dstr, box, swizzle)
+    src_h = datagen.random_bytes(sbytes, 5000 + len(name))
+    src = dev_bytes(src_h)
+    guard = 4096
+    out = dev_empty(dbytes + guard, fill=0x6C)
+    ms = atb.encode_tiled(dtype, src, sdims, sstr, box, swizzle)
+    md = atb.encode_tiled(dtype, out, ddims, dstr, box, swizzle)
+    if listed:
+        coords_h = datagen.random_box_origins(sdims, box, esize, 150, 5100 + len(name))
+        coords = dev_bytes(coords_h.view(np.uint8))
+        atb.tile_roundtrip(ms, md, coords, len(coords_h))
+    else:
+        coords_h = oracle.grid_coords(vs)
+        atb.tile_roundtrip(ms, md)
+    device_ok(atb)
+    want = np.full(dbytes + guard, 0x6C, dtype=np.uint8)
+    oracle.roundtrip(vs, src_h, vd, want, coords_h)
+    assert_bytes_equal(host(out), want, f"{name} {'listed' if listed else 'grid'} round trip")
