@@ -33,6 +33,8 @@ MUTANTS = {
     "oob_mask_unswizzled": ("image[oracle_swizzle(o, v->swizzle_bits)] = outside;", "image[o] = outside;"),
     "oob_mask_inverted": ("uint8_t outside = element_in_bounds(v, c, e, g) ? 0 : 1;",
                           "uint8_t outside = element_in_bounds(v, c, e, g) ? 1 : 0;"),
+    "roundtrip_stores_through_source_view": ("    oracle_tile_store(dst, dst_base, coords, n, packed);\n    free(packed);\n    return 0;\n}\n\n/*",
+                                             "    oracle_tile_store(src, dst_base, coords, n, packed);\n    free(packed);\n    return 0;\n}\n\n/*"),
     "add_subtracts": ("x = x + addend;", "x = x - addend;"),
     "roundtrip_skips_store": ("    oracle_tile_store(dst, dst_base, coords, n, packed);\n    free(packed);\n    return 0;\n}\n\n/*",
                               "    free(packed);\n    return 0;\n}\n\n/*"),

@@ -486,3 +486,25 @@ def test_oob_mask_marks_whole_elements_and_a_box_outside_is_all_fill():
     assert ((mask.min(axis=3) == mask.max(axis=3))).all()  # all 8 bytes of an element agree
     assert mask[1].all() and mask[2].all()  # entirely left of / below the tensor
     np.testing.assert_array_equal(mask[0, :, :, 0], [[0, 0, 1, 1], [0, 0, 1, 1], [1, 1, 1, 1], [1, 1, 1, 1]])
+
+
+def test_roundtrip_between_different_views_matches_numpy():
+    # source 13 x 9 f16 (row pitch 32 B), destination 11 x 7 f16 (row pitch 48 B); boxes 8 x 4
+    # in list order: later boxes overwrite earlier ones where they overlap
+    vs = oracle.View(2, (13, 9), (2, 32), (8, 4))
+    vd = oracle.View(2, (11, 7), (2, 48), (8, 4))
+    src = datagen.random_bytes(9 * 32, 61)
+    dst = np.full(7 * 48, 0xA5, dtype=np.uint8)
+    origins = np.array([(x, y) for y in (-2, 0, 3, 5, 8) for x in (-8, -4, 0, 4, 8, 12)], dtype=np.int32)
+    want = dst.copy()
+    a_dst = np_view(want, vd)  # [7, 11, 2] bytes, writable view into `want`
+    for o in origins:
+        img = np_box(src, vs, o)  # [4, 8, 2], zero outside the source
+        x0, y0 = int(o[0]), int(o[1])
+        for ky in range(4):
+            for kx in range(8):
+                y, x = y0 + ky, x0 + kx
+                if 0 <= y < 7 and 0 <= x < 11:
+                    a_dst[y, x] = img[ky, kx]
+    oracle.roundtrip(vs, src, vd, dst, origins)
+    np.testing.assert_array_equal(dst, want)
