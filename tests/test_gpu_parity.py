@@ -960,3 +960,14 @@ def test_round_trip_between_different_views(atb, case, listed):
     want = np.full(dbytes + guard, 0x6C, dtype=np.uint8)
     oracle.roundtrip(vs, src_h, vd, want, coords_h)
     assert_bytes_equal(host(out), want, f"{name} {'listed' if listed else 'grid'} round trip")
+
+    # the same move as two calls: gather from one view, store the images into the other
+    out2 = dev_empty(dbytes + guard, fill=0x6C)
+    md2 = atb.encode_tiled(dtype, out2, ddims, dstr, box, swizzle)
+    bb = atb.box_bytes(ms)
+    packed = dev_empty(len(coords_h) * bb, fill=0)
+    c_dev = dev_bytes(np.ascontiguousarray(coords_h, dtype=np.int32).view(np.uint8))
+    atb.tile_load(ms, c_dev, len(coords_h), packed)
+    atb.tile_store(md2, c_dev, len(coords_h), packed)
+    device_ok(atb)
+    assert_bytes_equal(host(out2), want, f"{name} gather then store")
