@@ -456,6 +456,18 @@ def workload_lines(torch, atb, datagen, device, stream, args):
     packed2 = torch.empty(n2 * bb2, dtype=torch.uint8, device=device)
     warm, cold = timed(lambda: atb.tile_load(ms2, None, 0, packed2, stream=stream), 300, 10)
     out["f32_16384x8192_step2_rows_gather"] = line(2 * n2 * bb2, n2, warm, cold)
+    del packed2
+    # the same 32x128 boxes given as a coordinate list (the grid's own origins, x fastest): the
+    # listed gather and the listed round trip read every origin from the list
+    gx, gy = np.meshgrid(np.arange(cols // 32, dtype=np.int32) * 32, np.arange(rows // 128, dtype=np.int32) * 128)
+    listed = torch.from_numpy(np.stack([gx.ravel(), gy.ravel()], 1).reshape(-1).copy()).to(device)
+    nl = listed.numel() // 2
+    packed_l = torch.empty(nl * atb.box_bytes(ma), dtype=torch.uint8, device=device)
+    warm, cold = timed(lambda: atb.tile_load(ma, listed, nl, packed_l, stream=stream), 300, 10)
+    out["f32_16384x8192_listed_gather"] = line(2 * rows * cols * 4, nl, warm, cold)
+    warm, cold = timed(lambda: atb.tile_roundtrip(ma, mb, listed, nl, stream=stream), 300, 10)
+    out["f32_16384x8192_listed_roundtrip"] = line(2 * rows * cols * 4, nl, warm, cold)
+    del packed_l
     atb.check_device(stream)
     return out
 
