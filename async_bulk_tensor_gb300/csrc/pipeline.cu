@@ -733,24 +733,25 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
         const int kind = origin_error<R>(a, c) != 0 ? kStoreNothing : store_kind<R>(a, c);
         if (ADD && kind != kStoreNothing) {
             // generic-proxy update of the landed box; element order is irrelevant.
-            // Eight 16-byte chunks per thread at a time (a 16 KiB box is exactly
-            // one such pass), all loads issued before the first add, so one
-            // shared-memory latency is paid per pass instead of one per chunk.
+            // Sixteen 16-byte chunks per thread at a time (with two consumer
+            // warps a 16 KiB box is exactly one such pass), all loads issued
+            // before the first add, so one shared-memory latency is paid per
+            // pass instead of one per chunk.
             const uint32_t base = r.stage(s);
             uint32_t j = ct;
-            for (; j + 7 * CT < chunks; j += 8 * CT) {
-                float v[8][4];
+            for (; j + 15 * CT < chunks; j += 16 * CT) {
+                float v[16][4];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ptx::ld_shared_v4_f32(base + 16 * (j + u * CT), v[u]);
+                for (int u = 0; u < 16; ++u) ptx::ld_shared_v4_f32(base + 16 * (j + u * CT), v[u]);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 16; ++u) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) v[u][e] = __fadd_rn(v[u][e], addend);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ptx::st_shared_v4_f32(base + 16 * (j + u * CT), v[u]);
+                for (int u = 0; u < 16; ++u) ptx::st_shared_v4_f32(base + 16 * (j + u * CT), v[u]);
             }
-            for (; j < chunks; j += CT) {  // the rest of a box that is not a multiple of 8 x 16 x CT bytes
+            for (; j < chunks; j += CT) {  // the rest of a box that is not a multiple of 16 x 16 x CT bytes
                 float v[4];
                 ptx::ld_shared_v4_f32(base + 16 * j, v);
 #pragma unroll
