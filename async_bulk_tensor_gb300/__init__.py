@@ -52,6 +52,7 @@ class TensorMap(ctypes.Structure):
 
     _fields_ = [
         ("map", ctypes.c_ubyte * 128),
+        ("map_wide", ctypes.c_ubyte * 128),
         ("base", ctypes.c_uint64),
         ("dims", ctypes.c_uint64 * MAX_RANK),
         ("strides", ctypes.c_uint64 * MAX_RANK),
@@ -64,6 +65,7 @@ class TensorMap(ctypes.Structure):
         ("l2_promotion", ctypes.c_uint32),
         ("oob_fill", ctypes.c_uint32),
         ("box_bytes", ctypes.c_uint32),
+        ("wide_box0", ctypes.c_uint32),
         ("magic", ctypes.c_uint32),
     ]
 
@@ -123,6 +125,7 @@ def _load():
         "atb_tile_roundtrip": (S, [MapP, MapP, P, U64, LaunchP, P]),
         "atb_init_device": (S, []),
         "atb_device_status": (S, [P, ctypes.POINTER(DeviceReport)]),
+        "atb_status_block_allocated": (ctypes.c_int, []),
         "atb_set_wait_timeout_ns": (None, [U64]),
         "atb_selftest_wait_timeout": (S, [U64, P]),
         "atb_tile_roundtrip_noalloc": (S, [MapP, MapP, P, U64, LaunchP, P, ctypes.POINTER(DeviceReport)]),
@@ -350,6 +353,12 @@ def tile_roundtrip_noalloc(src: TensorMap, dst: TensorMap, coords=None, n: int =
 
 def init_device():
     _check(lib.atb_init_device(), "atb_init_device")
+
+
+def status_block_allocated() -> int:
+    """``atb_status_block_allocated``: 1 if this process's library has allocated
+    the current device's status block, 0 if not, -1 if no device is readable."""
+    return int(lib.atb_status_block_allocated())
 
 
 def device_status(stream=None) -> DeviceReport:

@@ -16,6 +16,9 @@ constexpr uint32_t kTransformThreads = 32 + kConsumerThreads;
 constexpr uint32_t kUpdateConsumerThreads = 64;  // wide kernel, fp32 update: warps 1..2 update the stage
 constexpr uint32_t kStageAlignSwizzled = 1024;  // one period of the 128-byte swizzle
 constexpr uint32_t kStageAlignPlain = 128;
+// The engine's out-of-bounds NaN fill: 0x7FF7 in every 16-bit half (a NaN of
+// f16, bf16, f32 and f64 alike).
+constexpr uint32_t kNanFillWord = 0x7FF77FF7u;
 
 // Device status block: the first error wins the code/block/tile/where slots,
 // `errors` counts all of them.

@@ -309,6 +309,25 @@ atb_status atb_encode_tiled(atb_tensor_map* out, atb_dtype dtype, uint32_t rank,
 
     static_assert(sizeof(CUtensorMap) == sizeof(out->map), "tensor map size");
     memcpy(out->map, &map, sizeof map);
+
+    // The second descriptor: box[0] widened by one 16-byte chunk, no swizzle,
+    // everything else the same.  A box starting off the 16-byte grid along x
+    // lies inside the wider box that starts at the origin rounded down to the
+    // grid, which the engine may copy.
+    const uint32_t wide0 = box[0] + 16 / esize;
+    if (wide0 <= 256) {
+        cuuint32_t wdim[ATB_MAX_RANK];
+        for (uint32_t d = 0; d < rank; ++d) wdim[d] = d == 0 ? wide0 : box[d];
+        alignas(64) CUtensorMap wmap;
+        r = fn(&wmap, dtype_to_cu(dtype), rank, gbase, gdim, gstride, wdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, static_cast<CUtensorMapL2promotion>(l2_promotion),
+               oob_fill == ATB_OOB_NAN ? CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA
+                                       : CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS) {
+            memcpy(out->map_wide, &wmap, sizeof wmap);
+            out->wide_box0 = wide0;
+        }
+    }
     out->base = reinterpret_cast<uint64_t>(gbase);
     for (uint32_t d = 0; d < rank; ++d) {
         out->dims[d] = dims[d];
@@ -342,6 +361,17 @@ atb_status atb_init_device(void)
     clear_error();
     DeviceStatus* st = nullptr;
     return device_status_block(&st);
+}
+
+int atb_status_block_allocated(void)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return -1;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    return g_status[dev] != nullptr ? 1 : 0;
 }
 
 atb_status atb_device_status(atb_stream_t stream, atb_device_report* report)

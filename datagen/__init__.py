@@ -164,20 +164,23 @@ def storage(w: Workload, seed: int | None = None) -> np.ndarray:
     raise ValueError(w.values)
 
 
-def random_box_origins(dims, box, esize: int, n: int, seed: int, align_bytes: int = 16) -> np.ndarray:
+def random_box_origins(dims, box, esize: int, n: int, seed: int, align_bytes: int = 0) -> np.ndarray:
     """``n`` box origins (int32, innermost first), each box touching the tensor.
 
     Along every dimension the origin is uniform in [-(box-1), dims-1], so about
-    a quarter of the boxes hang over an edge.  The innermost origin is drawn on
-    the ``align_bytes`` grid (a multiple of 16 bytes), the granularity at which
-    a tensor-map copy may start along the contiguous dimension.
+    a quarter of the boxes hang over an edge.  With ``align_bytes`` > 0 the
+    innermost origin is drawn on that grid instead (x * esize a multiple of
+    ``align_bytes``); by default every element offset is possible.
     """
     g = rng(seed)
     out = np.empty((n, len(dims)), dtype=np.int32)
-    q = max(1, align_bytes // esize)
-    lo0 = -((box[0] - 1) // q) * q
-    hi0 = ((dims[0] - 1) // q) * q
-    out[:, 0] = g.integers(lo0 // q, hi0 // q + 1, size=n) * q
+    if align_bytes:
+        q = max(1, align_bytes // esize)
+        lo0 = -((box[0] - 1) // q) * q
+        hi0 = ((dims[0] - 1) // q) * q
+        out[:, 0] = g.integers(lo0 // q, hi0 // q + 1, size=n) * q
+    else:
+        out[:, 0] = g.integers(-(box[0] - 1), dims[0], size=n)
     for d in range(1, len(dims)):
         out[:, d] = g.integers(-(box[d] - 1), dims[d], size=n)
     return out

@@ -14,10 +14,17 @@
  *     wrong order).  Coordinates are element offsets (int32) of a box's first
  *     element and may be negative or past the end: a load reads zero bytes
  *     there, a store drops those elements.
- *   - Along the innermost dimension a box origin must sit on a 16-byte
- *     boundary: x * element_size must be a multiple of 16.  Kernels check it
- *     per box; a violating box is skipped and ATB_ERR_COORD_ALIGN is recorded
- *     in the device status (see atb_device_status).
+ *   - Listed origins may be any int32 within +-2^30 (a box beyond that is
+ *     refused per box with ATB_ERR_COORD_RANGE in the device status).  The
+ *     tensor-map engine can start a copy along the innermost dimension only
+ *     on a 16-byte boundary (x * element_size a multiple of 16).  A listed box
+ *     whose origin is off that grid is loaded through the map's second,
+ *     one-chunk-wider descriptor (map_wide) from the origin rounded down to
+ *     the grid, and the kernel's consumer threads cut the box out of that
+ *     wider image (or, without map_wide, load it with plain loads); boxes
+ *     written to a tensor from such an origin leave through plain stores of
+ *     aligned 16-byte chunks.  The result is the same as for any other
+ *     origin.  Tile-grid origins are always on the grid.
  *   - A "packed" buffer holds n box images back to back, image i at byte
  *     offset i * box_bytes, each byte-for-byte the shared-memory image of that
  *     box as the engine writes it (swizzle applied, stage base aligned to the
@@ -82,7 +89,8 @@ typedef enum {
     ATB_ERR_ARG = 13,            /* a null pointer, zero extent, bad stride or mismatched maps */
     ATB_ERR_TIMEOUT = 14,        /* (device) an mbarrier wait ran out of time */
     ATB_ERR_CUDA = 15,           /* a CUDA runtime call failed */
-    ATB_ERR_COORD_ALIGN = 16,    /* (device) a box origin breaks the 16-byte rule along x */
+    ATB_ERR_COORD_ALIGN = 16,    /* not raised any more: off-grid origins along x are moved by
+                                    threads; the number stays reserved */
     ATB_ERR_COORD_RANGE = 17,    /* (device) a box origin is beyond +-2^30 */
     ATB_ERR_STRIDE_RANGE = 18,   /* a byte stride (dims 1..rank-1) is 0 or not below 2^40 */
     ATB_ERR_DIM_RANGE = 19,      /* an extent is 0 or above 2^32 */
@@ -125,6 +133,10 @@ typedef enum {
  */
 typedef struct {
     unsigned char map[128];
+    unsigned char map_wide[128];      /* the same tensor with box[0] one 16-byte chunk wider and no
+                                         swizzle: listed boxes whose x origin is off the 16-byte grid
+                                         are loaded through it from the origin rounded down to the
+                                         grid (see "Conventions") */
     uint64_t base;                    /* global address the map was encoded over */
     uint64_t dims[ATB_MAX_RANK];      /* innermost first */
     uint64_t strides[ATB_MAX_RANK];   /* byte strides; strides[0] = element size */
@@ -137,6 +149,9 @@ typedef struct {
     uint32_t l2_promotion;            /* atb_l2_promotion */
     uint32_t oob_fill;                /* atb_oob_fill */
     uint32_t box_bytes;               /* element size x product over d of ceil(box[d] / elem_strides[d]) */
+    uint32_t wide_box0;               /* box[0] of map_wide (box[0] + 16 / element size), or 0 when
+                                         there is none (box[0] would exceed 256, or the driver
+                                         refused it): off-grid boxes are then loaded by threads */
     uint32_t magic;                   /* set by atb_encode_tiled */
 } atb_tensor_map;
 
@@ -279,6 +294,10 @@ atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, s
  * one cp.async.bulk.tensor per box; one consumer thread waits on the stage's
  * phase and drains the landed image with a 1-D bulk store to
  * d_packed + i * box_bytes, recycling the stage after the bulk group's reads.
+ * Calls with a coordinate list run four consumer warps: a listed box whose x
+ * origin is off the 16-byte grid is armed with no bytes, and those warps
+ * build its image with plain loads (the fill value outside the tensor, the
+ * same bytes the engine writes) before it is drained.
  *
  *   src       encoded map of the source tensor
  *   d_coords  device array of n * rank int32 origins, innermost first; NULL =
@@ -306,9 +325,10 @@ atb_status atb_tile_load(const atb_tensor_map* src, const int32_t* d_coords, uin
  * wait_group.read.  Elements outside the tensor are not written.  A box whose
  * origin is negative in any dimension is written by the consumer threads with
  * plain clipped stores instead (a tensor store may not start before the
- * tensor), and so is a box that crosses the end of a row whose byte length
- * (dims[0] x element size) is not a multiple of 16: the engine writes the
- * last 16-byte chunk of such a row whole, which would spill past the row.
+ * tensor), and so is a box whose x origin is off the 16-byte grid, and a box
+ * that crosses the end of a row whose byte length (dims[0] x element size) is
+ * not a multiple of 16: the engine writes the last 16-byte chunk of such a
+ * row whole, which would spill past the row.
  * Calls with a coordinate list run four consumer warps, which share those
  * clipped stores; calls over the tile grid run one.
  * Boxes that overlap with different contents land in an unspecified order.
@@ -405,6 +425,13 @@ atb_status atb_init_device(void);
  * errors after the read; synchronise them first to include them.
  */
 atb_status atb_device_status(atb_stream_t stream, atb_device_report* report);
+
+/*
+ * Whether the current device's status block (see atb_init_device) has been
+ * allocated in this process: 1 yes, 0 no, -1 if the current device cannot be
+ * read.  Allocates nothing and launches nothing.
+ */
+int atb_status_block_allocated(void);
 
 /* Limit for every mbarrier wait inside the kernels, in nanoseconds of the
  * GPU's global timer (default 1e9 = one second).  0 restores the default. */

@@ -7,7 +7,7 @@ a permuted 3-D fp32 view with 4096 random, partly out-of-bounds boxes; the
 512 MiB fp16 round trip in the launch configuration the benchmark times),
 small multi-tile cases with ragged tails over every rank, element size and
 swizzle mode, and the edge cases (no boxes, one box, maximum box extents,
-misaligned origins, boxes entirely outside the tensor).
+origins off the 16-byte grid, boxes entirely outside the tensor).
 """
 import numpy as np
 import pytest
@@ -313,24 +313,118 @@ def test_zero_boxes_launch_nothing(atb):
     assert (host(packed) == 0xEE).all()
 
 
-def test_misaligned_origin_is_reported_and_skipped(atb):
-    v = oracle.View(2, (128, 64), (2, 256), (64, 16))
-    src_h = datagen.random_bytes(64 * 256, 90)
-    src = dev_bytes(src_h)
-    coords_h = np.array([[0, 0], [3, 16], [64, 32]], dtype=np.int32)  # x = 3 -> 6 bytes, not 16-aligned
-    coords = dev_bytes(coords_h.view(np.uint8))
-    ms = atb.encode_tiled("f16", src, v.dims, v.strides, v.box)
+# boxes whose x origin is off the 16-byte grid (the engine may not start a copy
+# there; the consumer threads move them): every phase of a 16-byte chunk, at
+# and across the start and the end of whole and ragged rows, and wholly outside
+OFF_GRID = [
+    # name, dtype, dims, box, swizzle, outer order
+    ("r1_u8", "u8", (1000,), (64,), "none", None),
+    ("r2_u8_ragged", "u8", (1001, 9), (48, 4), "none", None),
+    ("r2_f16_sw128", "f16", (300, 40), (64, 8), "128B", None),
+    ("r2_bf16_ragged_sw64", "bf16", (301, 33), (32, 5), "64B", None),
+    ("r2_f32_sw32", "f32", (130, 20), (8, 6), "32B", None),
+    ("r2_f32_box256", "f32", (600, 7), (256, 3), "none", None),
+    ("r2_f64_ragged", "f64", (51, 12), (8, 3), "none", None),
+    ("r3_f32_sw128_permuted", "f32", (70, 9, 6), (32, 4, 2), "128B", [2, 1]),
+    ("r4_f16_sw32", "f16", (45, 7, 5, 3), (16, 3, 2, 2), "32B", None),
+]
+
+
+def _off_grid_origins(dims, box, esize, seed):
+    q = 16 // esize
+    d0, b0 = dims[0], box[0]
+    xs = sorted(set(range(-b0 - q, -b0 + 2 * q)) | set(range(-2 * q, 2 * q + 1)) |
+                set(range(d0 - b0 - q, d0 - b0 + q + 1)) | set(range(d0 - 2 * q, d0 + q + 1)))
+    g = datagen.rng(seed)
+    c = np.empty((len(xs), len(dims)), dtype=np.int32)
+    c[:, 0] = xs
+    for d in range(1, len(dims)):
+        c[:, d] = g.integers(-(box[d] - 1), dims[d], size=len(xs))
+    c = np.concatenate([c, datagen.random_box_origins(dims, box, esize, 60, seed + 1)])
+    g.shuffle(c)
+    return c
+
+
+@pytest.mark.parametrize("case", OFF_GRID, ids=[c[0] for c in OFF_GRID])
+@pytest.mark.parametrize("launch", [dict(), dict(stages=1, ctas=1), dict(checks=1, stages=2, ctas=3)],
+                         ids=["default", "s1c1", "ring_check_s2c3"])
+def test_off_grid_origins_all_ops(atb, case, launch):
+    name, dtype, dims, box, swizzle, order = case
+    esize = datagen.ESIZE[dtype]
+    strides, nbytes = _strides(esize, dims, order=order)
+    v = oracle.View(esize, dims, strides, box, swizzle)
+    src_h = datagen.random_bytes(nbytes, 4100 + len(name))
+    coords_h = _off_grid_origins(dims, box, esize, 4200 + len(name))
+    assert ((coords_h[:, 0].astype(np.int64) * esize) % 16 != 0).mean() > 0.3
+    src, coords = dev_bytes(src_h), dev_bytes(coords_h.view(np.uint8))
+    n = len(coords_h)
+    ms = atb.encode_tiled(dtype, src, dims, strides, box, swizzle)
     bb = atb.box_bytes(ms)
-    packed = dev_empty(3 * bb, fill=0xEE)
-    atb.tile_load(ms, coords, 3, packed, stages=2, ctas=1)
-    rep = atb.device_status()
-    assert rep.code == atb.ATB_ERR_COORD_ALIGN and rep.tile == 1 and rep.errors == 1, rep.as_dict()
+    guard = 4096
+
+    packed = dev_empty(n * bb + guard, fill=0xEE)
+    atb.tile_load(ms, coords, n, packed, **launch)
+    device_ok(atb)
+    want_packed = oracle.tile_load(v, src_h, coords_h)
     got = host(packed)
-    want = oracle.tile_load(v, src_h, coords_h)
-    assert_bytes_equal(got[:bb], want[:bb], "box 0")
-    assert (got[bb:2 * bb] == 0xEE).all()  # skipped box left untouched
-    assert_bytes_equal(got[2 * bb:], want[2 * bb:], "box 2")
-    device_ok(atb)  # the report was reset by the previous read
+    assert_bytes_equal(got, want_packed, f"{name} gather", image_bytes=bb)
+    assert (got[n * bb:] == 0xEE).all(), f"{name} gather wrote past the packed buffer"
+
+    out = dev_empty(nbytes + guard, fill=0x5A)
+    md = atb.encode_tiled(dtype, out, dims, strides, box, swizzle)
+    atb.tile_store(md, coords, n, packed[: n * bb], **launch)
+    device_ok(atb)
+    want = np.full(nbytes + guard, 0x5A, dtype=np.uint8)
+    oracle.tile_store(v, want, coords_h, want_packed)
+    assert_bytes_equal(host(out), want, f"{name} store")
+
+    out2 = dev_empty(nbytes + guard, fill=0x33)
+    md2 = atb.encode_tiled(dtype, out2, dims, strides, box, swizzle)
+    atb.tile_roundtrip(ms, md2, coords, n, **launch)
+    device_ok(atb)
+    want2 = np.full(nbytes + guard, 0x33, dtype=np.uint8)
+    oracle.roundtrip(v, src_h, v, want2, coords_h)
+    assert_bytes_equal(host(out2), want2, f"{name} round trip")
+
+    if dtype == "f32":
+        fin_h = datagen.finite_f32_bytes(nbytes // 4, 4300 + len(name))
+        fin = dev_bytes(fin_h)
+        mf = atb.encode_tiled(dtype, fin, dims, strides, box, swizzle)
+        out3 = dev_empty(nbytes + guard, fill=0x44)
+        md3 = atb.encode_tiled(dtype, out3, dims, strides, box, swizzle)
+        atb.tile_roundtrip_add_f32(mf, md3, 1.0, coords, n, **launch)
+        device_ok(atb)
+        want3 = np.full(nbytes + guard, 0x44, dtype=np.uint8)
+        oracle.roundtrip_add_f32(v, fin_h, v, want3, coords_h, 1.0)
+        assert_bytes_equal(host(out3), want3, f"{name} fp32 update")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32", "f64"])
+def test_off_grid_nan_fill_matches_the_engine_fill(atb, dtype):
+    # Whether the engine or the consumer threads filled an element outside the
+    # tensor, its bytes are the same NaN (0x7FF7 in every 16-bit half).
+    esize = datagen.ESIZE[dtype]
+    q = 16 // esize
+    dims, box = (120 + 1, 9), (32 // esize * 2, 4)
+    strides, nbytes = _strides(esize, dims)
+    v = oracle.View(esize, dims, strides, box, "none")
+    src_h = datagen.random_bytes(nbytes, 4400)
+    xs = list(range(-box[0] - q, q + 1)) + list(range(dims[0] - box[0] - q, dims[0] + q))
+    coords_h = np.array([[x, y] for x in xs for y in (-3, 2, 7)], dtype=np.int32)
+    src, coords = dev_bytes(src_h), dev_bytes(coords_h.view(np.uint8))
+    ms = atb.encode_tiled(dtype, src, dims, strides, box, oob_fill="nan")
+    bb = atb.box_bytes(ms)
+    packed = dev_empty(len(coords_h) * bb, fill=0)
+    atb.tile_load(ms, coords, len(coords_h), packed)
+    device_ok(atb)
+    got = host(packed)
+    _check_nan_fill(got, v, src_h, coords_h, dtype, f"{dtype} off-grid NaN fill")
+    mask = oracle.tile_oob_mask(v, coords_h).reshape(len(coords_h), bb)
+    imgs = got.reshape(len(coords_h), bb)
+    on_grid = (coords_h[:, 0] * esize) % 16 == 0
+    for which, rows in (("engine", on_grid), ("threads", ~on_grid)):
+        filled = imgs[rows][mask[rows] == 1].reshape(-1, 2)
+        assert filled.size and (filled == np.array([0xF7, 0x7F], dtype=np.uint8)).all(), which
 
 
 def test_origin_beyond_range_is_reported_and_never_issued(atb):

@@ -293,13 +293,16 @@ def test_c3_edge_tiles_zero_counts():
     assert zeros[3] == (128 * 64 - valid_rows * valid_cols) * 2
 
 
-def test_c4_random_origins_touch_tensor_and_are_aligned():
+def test_c4_random_origins_touch_tensor_and_span_every_offset():
     w = datagen.C4
     c = datagen.workload_coords(w)
     assert c.shape == (4096, 3)
-    assert (c[:, 0] % 4 == 0).all()  # 16-byte granularity along the contiguous dimension
     for d in range(3):
         assert (c[:, d] + w.box[d] - 1 >= 0).all() and (c[:, d] < w.dims[d]).all()
+        assert c[:, d].min() == -(w.box[d] - 1) and c[:, d].max() == w.dims[d] - 1  # the whole range is drawn
+    # every element offset along x: all four 4-byte phases of a 16-byte chunk occur
+    phases = np.bincount(c[:, 0] % 4, minlength=4) / len(c)
+    assert (np.abs(phases - 0.25) < 0.04).all()
     partial = ((c[:, 0] < 0) | (c[:, 0] + 32 > 1024) | (c[:, 1] < 0) | (c[:, 1] + 64 > 512)).mean()
     assert 0.15 < partial < 0.4
 
