@@ -84,7 +84,8 @@ class Launch(ctypes.Structure):
         ("poll_suspend_ns", ctypes.c_uint32),
         ("prefetch_boxes", ctypes.c_uint32),
         ("checks", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32 * 2),
+        ("consumer", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32 * 1),
     ]
 
 
@@ -237,10 +238,14 @@ def _check(code: int, where: str):
 HINT_LOAD_EVICT_FIRST, HINT_STORE_EVICT_FIRST, HINT_STORE_EVICT_LAST = 1, 2, 4
 
 
+CONSUMERS = {"auto": 0, "drain": 1, "warp": 2}
+
+
 def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True,
-            poll_suspend_ns=0, prefetch_boxes=0, checks=0) -> Launch:
+            poll_suspend_ns=0, prefetch_boxes=0, checks=0, consumer="auto") -> Launch:
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
-                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes, checks)
+                  store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes, checks,
+                  CONSUMERS[consumer] if isinstance(consumer, str) else consumer)
 
 
 def version() -> int:

@@ -619,6 +619,13 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32
     const int64_t gstep1 = R > 1 ? static_cast<int64_t>(group) * a.step[1] : 0;
     const uint64_t stride1 = R > 1 ? a.dst_strides[1] : 0;
 
+    // the smem offset of chunk j of the row that starts at r_off
+    auto chunk_at = [&](uint32_t r_off, uint32_t j) {
+        const uint32_t o = r_off + 16 * j;
+        return stage + (o ^ (((o >> 7) & line_mask) << 4));
+    };
+    const bool pair = source == kFromImage && rb != 0;  // two image chunks make one destination chunk
+
     for (uint32_t plane = 0; plane < planes; ++plane) {
         uint32_t rest = plane;
         bool inside = true;
@@ -635,10 +642,50 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32
         // destination chunk 0 of the box's rows in this plane (it may lie
         // before the row: only bytes from in_lo on are ever written)
         uint8_t* chunk0 = a.dst_base + plane_addr + static_cast<uint64_t>(base_b);
+        const uint32_t plane_off = plane * rows1 * pitch;
+        if (cg <= nthreads) {
+            // One destination column per thread: its byte range, its image
+            // chunks and its whole-or-part decision are fixed for the box.
+            // Four rows at a time: their shared loads are issued before any
+            // shift or store.
+            const uint32_t m = m0;
+            const int64_t lo64 = in_lo - 16 * static_cast<int64_t>(m), hi64 = in_hi - 16 * static_cast<int64_t>(m);
+            if (hi64 <= 0 || lo64 >= 16) return;
+            const uint32_t lo = lo64 > 0 ? static_cast<uint32_t>(lo64) : 0u;
+            const uint32_t hi = hi64 < 16 ? static_cast<uint32_t>(hi64) : 16u;
+            const bool whole = lo == 0 && hi == 16;
+            const bool has_a = pair && m >= 1, has_b = !pair || m < cpr;
+            uint8_t* col = chunk0 + 16 * m;
+            constexpr int U = 4;
+            for (uint32_t k1 = first_row; k1 < rows1; k1 += U * group) {
+                uint4 A[U], B[U];
+                bool row_in[U];
+                uint8_t* dst[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t kk = k1 + u * group;
+                    const int64_t g1 = R > 1 ? static_cast<int64_t>(c[1]) + static_cast<int64_t>(kk) * a.step[1] : 0;
+                    row_in[u] = kk < rows1 && g1 >= 0 && g1 < dims1;
+                    dst[u] = col + static_cast<uint64_t>(row_in[u] ? g1 : 0) * stride1;
+                    const uint32_t r_off = plane_off + kk * pitch;
+                    A[u] = make_uint4(0, 0, 0, 0);
+                    B[u] = make_uint4(0, 0, 0, 0);
+                    if (row_in[u] && has_a) A[u] = ptx::ld_shared_v4_u32(chunk_at(r_off, m - 1));
+                    if (row_in[u] && has_b) B[u] = ptx::ld_shared_v4_u32(chunk_at(r_off, m));
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (!row_in[u]) continue;
+                    const uint4 v = pair ? bytes_from_pair(A[u], B[u], 16 - rb) : B[u];
+                    if (whole) *reinterpret_cast<uint4*>(dst[u]) = v;
+                    else st_global_part(dst[u], v, lo, hi);
+                }
+            }
+            continue;
+        }
         int64_t g1 = R > 1 ? static_cast<int64_t>(c[1]) + static_cast<int64_t>(first_row) * a.step[1] : 0;
-        uint32_t r_off = (plane * rows1 + first_row) * pitch;
+        uint32_t r_off = plane_off + first_row * pitch;
         const uint32_t r_step = group * pitch;
-#pragma unroll 2
         for (uint32_t k1 = first_row; k1 < rows1; k1 += group, g1 += gstep1, r_off += r_step) {
             if (g1 < 0 || g1 >= dims1) continue;
             uint8_t* row = chunk0 + static_cast<uint64_t>(g1) * stride1;
@@ -647,19 +694,11 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32
                 const int64_t hi = in_hi - 16 * static_cast<int64_t>(m);
                 if (hi <= 0 || lo >= 16) continue;
                 uint4 v;
-                if (source == kFromWide || rb == 0) {
-                    const uint32_t o = r_off + 16 * m;
-                    v = ptx::ld_shared_v4_u32(stage + (o ^ (((o >> 7) & line_mask) << 4)));
+                if (!pair) {
+                    v = ptx::ld_shared_v4_u32(chunk_at(r_off, m));
                 } else {
-                    uint4 A = make_uint4(0, 0, 0, 0), B = make_uint4(0, 0, 0, 0);
-                    if (m >= 1) {
-                        const uint32_t o = r_off + 16 * (m - 1);
-                        A = ptx::ld_shared_v4_u32(stage + (o ^ (((o >> 7) & line_mask) << 4)));
-                    }
-                    if (m < cpr) {
-                        const uint32_t o = r_off + 16 * m;
-                        B = ptx::ld_shared_v4_u32(stage + (o ^ (((o >> 7) & line_mask) << 4)));
-                    }
+                    const uint4 A = m >= 1 ? ptx::ld_shared_v4_u32(chunk_at(r_off, m - 1)) : make_uint4(0, 0, 0, 0);
+                    const uint4 B = m < cpr ? ptx::ld_shared_v4_u32(chunk_at(r_off, m)) : make_uint4(0, 0, 0, 0);
                     v = bytes_from_pair(A, B, 16 - rb);
                 }
                 st_global_part(row + 16 * m, v, lo > 0 ? static_cast<uint32_t>(lo) : 0u,
@@ -687,14 +726,27 @@ __device__ void pack_from_wide(const PipeArgs& a, const int32_t (&c)[R], uint32_
     const uint32_t first_row = tid / cols;
     if (first_row >= group) return;
     const uint32_t j0 = tid - first_row * cols;
-#pragma unroll 2
-    for (uint32_t rho = first_row; rho < rows; rho += group) {
-        const uint32_t w_row = stage + rho * a.wide_pitch;
-        for (uint32_t j = j0; j < cpr; j += cols) {
-            const uint4 A = ptx::ld_shared_v4_u32(w_row + 16 * j);
-            const uint4 B = ptx::ld_shared_v4_u32(w_row + 16 * (j + 1));
-            const uint32_t o = rho * row_bytes + 16 * j;
-            *reinterpret_cast<uint4*>(slot + (o ^ (((o >> 7) & line_mask) << 4))) = bytes_from_pair(A, B, rb);
+    constexpr int U = 4;
+    for (uint32_t j = j0; j < cpr; j += cols) {
+        for (uint32_t rho = first_row; rho < rows; rho += U * group) {
+            uint4 A[U], B[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t r = rho + u * group;
+                if (r < rows) {
+                    const uint32_t w = stage + r * a.wide_pitch + 16 * j;
+                    A[u] = ptx::ld_shared_v4_u32(w);
+                    B[u] = ptx::ld_shared_v4_u32(w + 16);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t r = rho + u * group;
+                if (r < rows) {
+                    const uint32_t o = r * row_bytes + 16 * j;
+                    *reinterpret_cast<uint4*>(slot + (o ^ (((o >> 7) & line_mask) << 4))) = bytes_from_pair(A[u], B[u], rb);
+                }
+            }
         }
     }
 }
@@ -1296,6 +1348,7 @@ constexpr uint32_t kDefaultStages = 3;
 constexpr uint32_t kDefaultStoreGroups = 2;
 constexpr uint64_t kStageBytesPerSm = 96u * 1024u;
 constexpr uint64_t kMaxDefaultCtasPerSm = 8;
+constexpr uint32_t kDrainStageBytes = 32u * 1024u;
 
 uint32_t default_stages(const atb_tensor_map* m, const DeviceInfo& dev, bool wide_loads)
 {
@@ -1379,6 +1432,8 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     }
     if (cfg && (cfg->checks & ~ATB_CHECK_RING))
         return set_error(ATB_ERR_ARG, "unknown check bits 0x%x", cfg->checks & ~ATB_CHECK_RING);
+    if (cfg && cfg->consumer > ATB_CONSUMER_WARP)
+        return set_error(ATB_ERR_ARG, "unknown consumer %u", cfg->consumer);
     if (MODE == kLoad || MODE == kStore) {
         if (!packed) return set_error(ATB_ERR_ARG, "packed buffer is NULL");
         if (reinterpret_cast<uintptr_t>(packed) % 16)
@@ -1428,16 +1483,21 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     // several consumer warps; tile-grid launches run the 64-thread kernel.
     constexpr int kBase = MODE == kRoundtripAddF32 ? kRoundtrip : MODE;
     const bool wide = MODE == kRoundtripAddF32 || coords != nullptr;
-    // Tile grid: the one-thread drain wherever every box leaves through one
-    // engine copy (no box misses the destination or crosses a ragged row end);
-    // the warp consumer, which can also write plain clipped stores, otherwise.
+    // Tile grid: where every box leaves through one engine copy (no box misses
+    // the destination or crosses a ragged row end) either consumer serves; the
+    // library takes the one-thread drain for stages of 32 KiB and more and the
+    // warp consumer below (measured on GB300: each was the faster there, and
+    // the warp consumer's lead below 32 KiB held in every build measured).
+    // The warp consumer, which can also write plain clipped stores, otherwise.
     bool plain = false;
     if (!wide && MODE != kLoad) {
         plain = (dst->dims[0] * dst->esize) % 16 != 0;
         if (MODE == kRoundtrip)
             for (uint32_t d = 0; d < rank; ++d) plain = plain || dst->dims[d] < src->dims[d];
     }
-    const bool drain = !wide && !plain;
+    const uint32_t consumer = cfg ? cfg->consumer : ATB_CONSUMER_AUTO;
+    const bool drain = !wide && !plain &&
+                       (consumer == ATB_CONSUMER_DRAIN || (consumer == ATB_CONSUMER_AUTO && stage_b >= kDrainStageBytes));
     WideKernelFn wide_fn = nullptr;
     KernelFn grid_fn = nullptr;
     if (MODE == kRoundtripAddF32) wide_fn = wide_kernel_for_rank<kRoundtrip, true>(rank);

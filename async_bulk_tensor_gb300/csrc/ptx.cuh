@@ -132,50 +132,6 @@ __device__ __forceinline__ void st_shared_v4_u32(uint32_t addr, const uint4& v)
                  : "memory");
 }
 
-__device__ __forceinline__ void st_shared_u8(uint32_t addr, uint16_t v)
-{
-    asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
-{
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v)
-{
-    asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
-}
-
-// ---- thread-issued async copies (cp.async), completion on an mbarrier ---------
-// Global -> shared copy of 4 or 8 bytes, both addresses aligned to the size;
-// bytes past `src_bytes` (0..size) are written as zero and not read.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-// Raises the pending arrival count of `bar` by one now, and arrives on it once
-// every cp.async this thread issued before has completed.
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // ---- plain global loads through the read-only path ---------------------------
 // Used only on tensors no thread of the launch writes.  Volatile, so that a
 // batch of them stays ahead of the shared-memory stores that consume it.
@@ -185,34 +141,6 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p)
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(reinterpret_cast<uint64_t>(p)));
-    return v;
-}
-
-__device__ __forceinline__ uint16_t ld_global_nc_u8(const void* p)
-{
-    uint16_t v;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(reinterpret_cast<uint64_t>(p)));
-    return v;
-}
-
-__device__ __forceinline__ uint16_t ld_global_nc_u16(const void* p)
-{
-    uint16_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(reinterpret_cast<uint64_t>(p)));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_global_nc_u32(const void* p)
-{
-    uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(p)));
-    return v;
-}
-
-__device__ __forceinline__ uint64_t ld_global_nc_u64(const void* p)
-{
-    uint64_t v;
-    asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(v) : "l"(reinterpret_cast<uint64_t>(p)));
     return v;
 }
 

@@ -280,6 +280,7 @@ def run_gpu(args):
         "stages": args.stages or "library default (3)",
         "ctas_per_sm": args.ctas_per_sm or "library default (96 KiB of stages per SM)",
         "store_groups": "library default (2)", "launch": "programmatic dependent launch",
+        "consumer": "library default (warp consumer below 32 KiB stages, one-thread drain from 32 KiB)",
         "parallelism": f"replicas x{world}",
         "l2": "inputs larger than L2 (512 MiB read + 512 MiB written per step); no flush",
     }
@@ -314,31 +315,60 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+SMEM_PER_SM = 228 * 1024  # GB300: shared memory one SM can hold for resident CTAs
+
+
 def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
+    """Workload 5 over ring shapes.  Every cell names its launch shape: stages,
+    CTAs per SM, store groups in flight and KiB of stages per SM.  Rows:
+      default_rule   stages 2/3/4/6/8, CTAs per SM from the library's rule
+                     (about 96 KiB of stages per SM), two store groups;
+      fixed_96KiB    about 96 KiB of stages per SM, split between more stages
+                     and fewer CTAs or the reverse;
+      ctas_1, ctas_2 CTAs per SM held at one or two while the ring deepens.
+    A shape that does not fit one CTA's shared memory is reported as infeasible."""
     out = {}
     steps = max(50, min(400, args.steps // 10))
     for w, box in ((datagen.C5A, "64x256"), (datagen.C5B, "128x64_sw128")):
         ms = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle)
         md = atb.encode_tiled(w.dtype, dst, w.dims, w.strides, w.box, w.swizzle)
-        for stages in (2, 3, 4, 6, 8):
-            key = f"{box}_s{stages}"
+        stage_kib = atb.box_bytes(ms) // 1024
+
+        def cell(stages, per_sm, groups=2):
             try:
-                atb.pipeline_smem_bytes(ms, stages)
+                smem = atb.pipeline_smem_bytes(ms, stages)
             except atb.AtbError as e:
-                out[key] = f"infeasible: {e.name}"
-                continue
-            s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, stages=stages),
-                              steps, 5)
-            out[key] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
+                return f"infeasible: {e.name}"
+            if smem * per_sm > SMEM_PER_SM:
+                return f"infeasible: {per_sm} CTAs of {smem} bytes exceed the SM's shared memory"
+            g = min(groups, stages)
+            sec = time_launches(torch, stream, lambda: atb.tile_roundtrip(
+                ms, md, stream=stream, stages=stages, ctas_per_sm=per_sm, store_groups=g), steps, 5)
+            return {"GBps": round(2 * w.storage_bytes * steps / sec / 1e9, 1), "stages": stages, "ctas_per_sm": per_sm,
+                    "store_groups": g, "kib_per_sm": stages * stage_kib * per_sm}
+
+        rows = {"default_rule": {}, "fixed_96KiB": {}, "ctas_1": {}, "ctas_2": {}}
+        for stages in (2, 3, 4, 6, 8):
+            rule = max(1, min(8, (96 * 1024) // (stages * atb.box_bytes(ms))))
+            rows["default_rule"][f"s{stages}"] = cell(stages, rule)
+        for stages in (1, 2, 3, 6):
+            per_sm = (96 * 1024) // (stages * atb.box_bytes(ms))
+            if per_sm >= 1 and stages * per_sm * atb.box_bytes(ms) == 96 * 1024:
+                rows["fixed_96KiB"][f"s{stages}c{per_sm}"] = cell(stages, per_sm)
+        for per_sm, key in ((1, "ctas_1"), (2, "ctas_2")):
+            for stages in (2, 3, 4, 6, 8, 12):
+                rows[key][f"s{stages}"] = cell(stages, per_sm)
+        out[box] = rows
+        extra = {}
         for promo in ("128B", "256B"):  # L2 promotion of the source map, default pipeline
             mp = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle, promo)
-            s = time_launches(torch, stream, lambda: atb.tile_roundtrip(mp, md, stream=stream), steps, 5)
-            out[f"{box}_s3_l2promotion{promo}"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
-        s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, pdl=False), steps, 5)
-        out[f"{box}_s3_without_pdl"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
-        s = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, checks=atb.CHECK_RING),
-                          steps, 5)
-        out[f"{box}_s3_ring_check"] = round(2 * w.storage_bytes * steps / s / 1e9, 1)
+            sec = time_launches(torch, stream, lambda: atb.tile_roundtrip(mp, md, stream=stream), steps, 5)
+            extra[f"l2promotion{promo}"] = round(2 * w.storage_bytes * steps / sec / 1e9, 1)
+        for name, kw in (("without_pdl", dict(pdl=False)), ("ring_check", dict(checks=atb.CHECK_RING)),
+                         ("consumer_drain", dict(consumer="drain")), ("consumer_warp", dict(consumer="warp"))):
+            sec = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, **kw), steps, 5)
+            extra[name] = round(2 * w.storage_bytes * steps / sec / 1e9, 1)
+        out[box]["library_default_variants"] = extra
     return out
 
 
@@ -417,26 +447,37 @@ def workload_lines(torch, atb, datagen, device, stream, args):
     warm, cold = timed(lambda: atb.tile_load(ms, None, 0, packed, stream=stream), 500, 30)
     out[w.name] = line(10000 * 3000 * 2 + n * atb.box_bytes(ms), n, warm, cold)
 
-    # 4: 4096 random boxes of a permuted 3-D fp32 view: gather, then store
+    # 4: 4096 random boxes of a permuted 3-D fp32 view: gather, then store.  The
+    # workload's origins are uniform over every element offset (three in four
+    # boxes start off the 16-byte grid along x); the same count of origins drawn
+    # on the 16-byte grid is timed beside them.
     w = datagen.C4
-    coords_h = datagen.workload_coords(w)
     src = dev_bytes(datagen.storage(w))
-    coords = dev_bytes(coords_h.view(np.uint8))
     ms = atb.encode_tiled(w.dtype, src, w.dims, w.strides, w.box, w.swizzle)
     bb = atb.box_bytes(ms)
-    n = len(coords_h)
-    packed = torch.empty(n * bb, dtype=torch.uint8, device=device)
     fresh = torch.full((w.storage_bytes,), 0xFF, dtype=torch.uint8, device=device)
     mf = atb.encode_tiled(w.dtype, fresh, w.dims, w.strides, w.box, w.swizzle)
-    inb = box_inbound_bytes(w.dims, w.box, w.esize, coords_h)
-    warm, cold = timed(lambda: atb.tile_load(ms, coords, n, packed, stream=stream), 500, 30)
-    out[w.name + "_load"] = line(inb + n * bb, n, warm, cold)
-    for pf in (4, 16):
-        warm, cold = timed(lambda: atb.tile_load(ms, coords, n, packed, stream=stream, prefetch_boxes=pf), 500, 30)
-        out[w.name + f"_load_prefetch{pf}"] = line(inb + n * bb, n, warm, cold)
-    warm, cold = timed(lambda: atb.tile_store(mf, coords, n, packed, stream=stream), 500, 30)
-    out[w.name + "_store"] = line(n * bb + inb, n, warm, cold)
-    del src, packed, fresh
+    for tag, coords_h in (("", datagen.workload_coords(w)),
+                          ("_grid16B_origins", datagen.random_box_origins(w.dims, w.box, w.esize, w.n_random,
+                                                                         w.seed + 1000, align_bytes=16))):
+        coords = dev_bytes(coords_h.view(np.uint8))
+        n = len(coords_h)
+        packed = torch.empty(n * bb, dtype=torch.uint8, device=device)
+        inb = box_inbound_bytes(w.dims, w.box, w.esize, coords_h)
+        warm, cold = timed(lambda: atb.tile_load(ms, coords, n, packed, stream=stream), 500, 30)
+        out[w.name + tag + "_load"] = line(inb + n * bb, n, warm, cold)
+        if not tag:
+            for pf in (4, 16):
+                warm, cold = timed(lambda: atb.tile_load(ms, coords, n, packed, stream=stream, prefetch_boxes=pf),
+                                   500, 30)
+                out[w.name + f"_load_prefetch{pf}"] = line(inb + n * bb, n, warm, cold)
+        warm, cold = timed(lambda: atb.tile_store(mf, coords, n, packed, stream=stream), 500, 30)
+        out[w.name + tag + "_store"] = line(n * bb + inb, n, warm, cold)
+        warm, cold = timed(lambda: atb.tile_roundtrip(ms, mf, coords, n, stream=stream), 500, 30)
+        out[w.name + tag + "_roundtrip"] = line(2 * inb, n, warm, cold)
+        del packed
+    out["fixed_cost_fits"] = fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src, ms)
+    del src, fresh
 
     # the fp32 update between load and store: 16384 x 8192 fp32 (512 MiB), box 32x128, 128B swizzle
     rows, cols = 8192, 16384
@@ -469,6 +510,74 @@ def workload_lines(torch, atb, datagen, device, stream, args):
     out["f32_16384x8192_listed_roundtrip"] = line(2 * rows * cols * 4, nl, warm, cold)
     del packed_l
     atb.check_device(stream)
+    return out
+
+
+def fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src4, ms4):
+    """Each short launch as T(n) = T0 + n * t: the same launch over n boxes for
+    several n, timed after an L2 flush, and a least-squares line through the
+    points.  T0 is what a launch costs before and around its boxes (launch,
+    ramp-up of the first DRAM reads, drain of the last stores); bytes per box
+    / t is the rate the kernel sustains in between.  Fractions are of the
+    measured copy peak."""
+    import numpy as np
+
+    peak, _ = hbm_peak()
+
+    def fit(label, ns, bytes_per_box, make_fn):
+        pts = []
+        for n in ns:
+            _, cold = timed(make_fn(n), 20, 20)
+            pts.append((n, cold))
+        x = np.array([p[0] for p in pts], dtype=np.float64)
+        y = np.array([p[1] for p in pts], dtype=np.float64)
+        t, t0 = np.polyfit(x, y, 1)
+        full = pts[-1]
+        return {"points_us": {int(n): round(c * 1e6, 2) for n, c in pts}, "fixed_us": round(t0 * 1e6, 2),
+                "marginal_GBps": round(bytes_per_box / t / 1e9, 1),
+                "marginal_frac_of_peak": round(bytes_per_box / t / 1e9 / peak, 3),
+                "full_launch_frac_of_peak": round(full[0] * bytes_per_box / full[1] / 1e9 / peak, 3),
+                "full_launch_net_of_fixed_frac": round(full[0] * bytes_per_box / (full[1] - t0) / 1e9 / peak, 3),
+                "what": label}
+
+    w = datagen.C4
+    coords_h = datagen.workload_coords(w)
+    coords = dev_bytes(coords_h.view(np.uint8))
+    bb = atb.box_bytes(ms4)
+    packed = torch.empty(len(coords_h) * bb, dtype=torch.uint8, device=device)
+    inb_per_box = box_inbound_bytes(w.dims, w.box, w.esize, coords_h) / len(coords_h)
+    out = {"c4_gather": fit("workload 4 gather, first n of its 4096 listed boxes", (512, 1024, 2048, 3072, 4096),
+                            inb_per_box + bb,
+                            lambda n: (lambda: atb.tile_load(ms4, coords, n, packed, stream=stream)))}
+    # workload 2 over its first rows: the same 64 x 256 boxes, n = 7 column tiles x row strips
+    w = datagen.C2
+    src2 = dev_bytes(datagen.storage(w))
+    dst2 = torch.zeros(w.storage_bytes, dtype=torch.uint8, device=device)
+    maps = {}
+    for strips in (16, 33, 66, 99, 132):
+        rows = strips * 64
+        maps[strips * 7] = (atb.encode_tiled(w.dtype, src2, (w.dims[0], rows), w.strides, w.box, w.swizzle),
+                            atb.encode_tiled(w.dtype, dst2, (w.dims[0], rows), w.strides, w.box, w.swizzle))
+    out["c2_round_trip"] = fit("workload 2 round trip over its first row strips (library grid)", sorted(maps),
+                               2 * 64 * 256 * 2,
+                               lambda n: (lambda: atb.tile_roundtrip(maps[n][0], maps[n][1], stream=stream)))
+    # host side of one call: ctypes marshalling and the library's launch, with the GPU kept busy
+    busy = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    w = datagen.C1
+    s1 = dev_bytes(datagen.storage(w))
+    d1 = torch.zeros_like(s1)
+    m1s = atb.encode_tiled(w.dtype, s1, w.dims, w.strides, w.box, w.swizzle)
+    m1d = atb.encode_tiled(w.dtype, d1, w.dims, w.strides, w.box, w.swizzle)
+    with torch.cuda.stream(stream):
+        for _ in range(4):
+            busy.zero_()
+        t0 = time.perf_counter()
+        for _ in range(200):
+            atb.tile_roundtrip(m1s, m1d, stream=stream, stages=1, ctas=1)
+        host = (time.perf_counter() - t0) / 200
+    stream.synchronize()
+    out["host_us_per_call"] = {"value": round(host * 1e6, 2),
+                               "what": "Python binding + library enqueue of one round-trip call (CPU clock, GPU busy)"}
     return out
 
 

@@ -170,8 +170,27 @@ typedef struct {
     uint32_t prefetch_boxes;  /* tensor loads: prefetch the box this many boxes ahead into L2 with
                                  cp.async.bulk.prefetch.tensor (0 = off) */
     uint32_t checks;          /* ATB_CHECK_* bits: consistency checks inside the kernel (0 = none) */
-    uint32_t reserved[2];
+    uint32_t consumer;        /* tile-grid launches: ATB_CONSUMER_* (0 = the library's choice) */
+    uint32_t reserved[1];
 } atb_launch;
+
+/*
+ * atb_launch.consumer, for launches over the tile grid whose every box leaves
+ * through one engine copy (gathers; stores and round trips whose destination
+ * holds the whole grid and whose rows end on 16-byte boundaries).  Other
+ * launches ignore it.
+ *   ATB_CONSUMER_AUTO   the library's choice: the warp consumer for stages
+ *                       below 32 KiB, the one-thread drain from 32 KiB up
+ *                       (the faster of the two for each size on GB300)
+ *   ATB_CONSUMER_DRAIN  one consumer thread per CTA waits for each stage and
+ *                       issues its drain copy; fewest instructions per box
+ *   ATB_CONSUMER_WARP   a consumer warp follows every box and its lane 0
+ *                       issues the drain copy (the consumer that can also
+ *                       write boxes with plain clipped stores)
+ */
+#define ATB_CONSUMER_AUTO  0u
+#define ATB_CONSUMER_DRAIN 1u
+#define ATB_CONSUMER_WARP  2u
 
 /*
  * atb_launch.checks bits.

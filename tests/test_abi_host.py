@@ -110,7 +110,7 @@ def test_null_maps_are_rejected_without_a_device(atb):
 
 
 
-def test_unknown_check_bits_are_rejected_before_any_device_work(atb):
+def test_unknown_launch_options_are_rejected_before_any_device_work(atb):
     # a map record that passes the library's validity check (magic and rank);
     # the launch must refuse the unknown bit before asking for a device
     m = atb.TensorMap()
@@ -122,6 +122,9 @@ def test_unknown_check_bits_are_rejected_before_any_device_work(atb):
     with pytest.raises(atb.AtbError) as e:
         atb.tile_roundtrip(m, m, checks=2)
     assert e.value.code == atb.ATB_ERR_ARG and "check bits" in str(e.value)
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_roundtrip(m, m, consumer=3)
+    assert e.value.code == atb.ATB_ERR_ARG and "consumer" in str(e.value)
 
 
 class _FakeDeviceTensor:

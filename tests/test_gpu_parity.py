@@ -145,6 +145,16 @@ def test_c5_full_round_trip_default_launch(atb, w, c5_input, c5_device):
     assert_bytes_equal(host(dst), want, w.name, view=v)
 
 
+@pytest.mark.parametrize("consumer", ["drain", "warp"])
+@pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
+def test_c5_full_round_trip_each_consumer(atb, w, consumer, c5_input, c5_device):
+    dst = dev_empty(w.storage_bytes, fill=0)
+    ms, md = encode(atb, w, c5_device), encode(atb, w, dst)
+    atb.tile_roundtrip(ms, md, consumer=consumer)
+    device_ok(atb)
+    assert_bytes_equal(host(dst), c5_input, f"{w.name} {consumer}", view=oracle_view(w))
+
+
 @pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
 def test_c5_ring_check_full_size(atb, w, c5_input, c5_device):
     # the stage bookkeeping check over every box of the 512 MiB round trip, in
@@ -231,9 +241,10 @@ def _small_case(name, dtype, dims, box, swizzle, order, seed):
 @pytest.mark.parametrize("launch", [dict(stages=1, ctas=1), dict(stages=3, ctas=5, store_groups=2),
                                     dict(stages=2, ctas=3, schedule="contiguous"), dict(),
                                     dict(prefetch_boxes=3, l2_hints=3, poll_suspend_ns=20000),
-                                    dict(checks=1), dict(checks=1, stages=2, ctas=3, store_groups=2)],
+                                    dict(checks=1), dict(checks=1, stages=2, ctas=3, store_groups=2),
+                                    dict(consumer="drain"), dict(consumer="warp", stages=2, store_groups=1)],
                          ids=["s1c1", "s3c5g2", "s2c3contig", "default", "prefetch3_hints", "ring_check",
-                              "ring_check_s2c3g2"])
+                              "ring_check_s2c3g2", "drain", "warp_s2g1"])
 def test_small_cases_all_ops(atb, case, launch):
     name, dtype, dims, box, swizzle, order = case
     v, src_h, nbytes, coords_h = _small_case(name, dtype, dims, box, swizzle, order, 1000 + len(name))
