@@ -111,6 +111,18 @@ class View:
         assert len(self.strides) == self.rank and len(self.box) == self.rank
         assert self.strides[0] == self.esize
         assert self.estr is None or (len(self.estr) == self.rank and self.estr[0] == 1)
+        # The swizzle keeps every 16-byte chunk inside its 128-byte line; an
+        # image whose last line holds a number of chunks the XOR does not map
+        # onto itself would send chunks past the end of the box.  Such a view
+        # has no image of box_bytes bytes, and is refused before any C call.
+        bits = SWIZZLE_BITS[self.swizzle]
+        visited = self.esize
+        for d in range(self.rank):
+            e = self.estr[d] if self.estr is not None else 1
+            visited *= (int(self.box[d]) + e - 1) // e
+        if bits and visited % (16 << bits) != 0:
+            raise ValueError(f"a {self.swizzle} swizzle needs box bytes that are a multiple of {16 << bits}, "
+                             f"not {visited}")
 
     def _c(self) -> _View:
         v = _View()

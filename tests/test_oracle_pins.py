@@ -511,3 +511,14 @@ def test_roundtrip_between_different_views_matches_numpy():
                     a_dst[y, x] = img[ky, kx]
     oracle.roundtrip(vs, src, vd, dst, origins)
     np.testing.assert_array_equal(dst, want)
+
+
+def test_swizzled_view_whose_image_would_overflow_is_refused():
+    # The swizzle keeps chunks inside their 128-byte line: a 128B-swizzled box
+    # of 144 bytes (nine 16-byte rows) would move its last chunk past the box.
+    with pytest.raises(ValueError):
+        oracle.View(4, (8, 9, 7), (4, 32, 288), (4, 3, 3), "128B")
+    with pytest.raises(ValueError):
+        oracle.View(2, (8, 9), (2, 16), (8, 3), "64B")  # 48 bytes under a 64-byte period
+    assert oracle.box_bytes(oracle.View(2, (8, 9), (2, 16), (8, 4), "64B")) == 64
+    assert oracle.box_bytes(oracle.View(1, (48, 9), (1, 48), (48, 3), "none")) == 144
