@@ -323,6 +323,17 @@ __device__ __forceinline__ uint4 bytes_from_pair(const uint4& A, const uint4& B,
                       __funnelshift_r(t[2], t[3], sh), __funnelshift_r(t[3], t[4], sh));
 }
 
+// Bytes 4 S + b / 8 ... of the 32 bytes A then B (b = 8 x the shift's byte
+// part, 0..24), for a shift whose word part S is known at compile time: four
+// funnel shifts and no selects.
+template <int S>
+__device__ __forceinline__ uint4 shift_pair(const uint4& A, const uint4& B, uint32_t b)
+{
+    const uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+    return make_uint4(__funnelshift_r(w[S], w[S + 1], b), __funnelshift_r(w[S + 1], w[S + 2], b),
+                      __funnelshift_r(w[S + 2], w[S + 3], b), __funnelshift_r(w[S + 3], w[S + 4], b));
+}
+
 // Keeps bytes [lo, hi) of v (0 <= lo <= hi <= 16) and puts the fill's bytes
 // elsewhere.  Element boundaries are multiples of the element size and the
 // fill repeats every element, so the result is whole elements of either.
@@ -711,22 +722,24 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32
 // A gather's packed image of a box that the wider map loaded: image chunk
 // (row, j) is bytes rb + 16 j ... rb + 16 j + 15 of the wider row, shifted
 // out of two aligned chunks, and goes to its swizzled place in the box's slot
-// of the packed buffer.  `nthreads` threads as `group` rows of `cols` chunks.
-template <int R>
-__device__ void pack_from_wide(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage, uint8_t* slot, uint32_t tid,
-                               uint32_t nthreads)
+// of the packed buffer.  `nthreads` threads as `group` rows of `cols` chunks;
+// the shift is the same for the whole box, and its word part S is fixed at
+// compile time (pack_from_wide dispatches once per box).
+template <int R, int S>
+__device__ void pack_from_wide_s(const PipeArgs& a, uint32_t rb, uint32_t stage, uint8_t* slot, uint32_t tid,
+                                 uint32_t nthreads)
 {
     const uint32_t row_bytes = a.box[0] * a.esize;
     const uint32_t cpr = row_bytes / 16;
     const uint32_t rows = a.box_bytes / row_bytes;
-    const uint32_t rb = row_phase<R>(a, c);
     const uint32_t line_mask = (1u << a.swizzle_bits) - 1u;
+    const uint32_t bits = 8 * (rb & 3u);
     const uint32_t cols = cpr < nthreads ? cpr : nthreads;
     const uint32_t group = nthreads / cols;
     const uint32_t first_row = tid / cols;
     if (first_row >= group) return;
     const uint32_t j0 = tid - first_row * cols;
-    constexpr int U = 4;
+    constexpr int U = 2;
     for (uint32_t j = j0; j < cpr; j += cols) {
         for (uint32_t rho = first_row; rho < rows; rho += U * group) {
             uint4 A[U], B[U];
@@ -744,10 +757,24 @@ __device__ void pack_from_wide(const PipeArgs& a, const int32_t (&c)[R], uint32_
                 const uint32_t r = rho + u * group;
                 if (r < rows) {
                     const uint32_t o = r * row_bytes + 16 * j;
-                    *reinterpret_cast<uint4*>(slot + (o ^ (((o >> 7) & line_mask) << 4))) = bytes_from_pair(A[u], B[u], rb);
+                    *reinterpret_cast<uint4*>(slot + (o ^ (((o >> 7) & line_mask) << 4))) =
+                        shift_pair<S>(A[u], B[u], bits);
                 }
             }
         }
+    }
+}
+
+template <int R>
+__device__ void pack_from_wide(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage, uint8_t* slot, uint32_t tid,
+                               uint32_t nthreads)
+{
+    const uint32_t rb = row_phase<R>(a, c);
+    switch (rb >> 2) {
+    case 0: pack_from_wide_s<R, 0>(a, rb, stage, slot, tid, nthreads); break;
+    case 1: pack_from_wide_s<R, 1>(a, rb, stage, slot, tid, nthreads); break;
+    case 2: pack_from_wide_s<R, 2>(a, rb, stage, slot, tid, nthreads); break;
+    default: pack_from_wide_s<R, 3>(a, rb, stage, slot, tid, nthreads); break;
     }
 }
 
@@ -1136,7 +1163,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
 //   !ADD  gathers, stores and round trips over a coordinate list: four
 //         consumer warps.
 template <int MODE, int R, bool ADD>
-__global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumerThreads), ADD ? 1 : 4)
+__global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumerThreads), ADD ? 1 : (MODE == kLoad ? 3 : 4))
     tile_wide_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
                      const __grid_constant__ CUtensorMap wide_map, const PipeArgs a, float addend)
 {
@@ -1174,20 +1201,23 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
     bool failed = false;
     for (; k < count; ++k, cur.advance(a, S)) {
         const uint32_t s = cur.stage;
-        const bool ok = wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
-        if (!__all_sync(0xffffffffu, ok)) {
-            failed = true;
-        }
-        // Every consumer thread reads the origin slot before the barrier
-        // below; consumer thread 0 frees the stage only after that barrier, so
-        // no thread can see the slot refilled for a later box.
-        int32_t c[R];
-        landed_origin<R>(a, r, s, cur, c);
-        // every consumer warp must agree before any of them leaves the loop
-        if (ptx::named_barrier_or(1, CT, failed)) {
+        // Consumer thread 0 alone polls the stage's barrier; the others wait at
+        // the named barrier, which takes no issue slots, and learn its outcome
+        // through the barrier's OR.
+        const bool ok = ct != 0 || wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
+        if (ptx::named_barrier_or(1, CT, !ok)) {
             failed = true;
             break;
         }
+        // The phase is complete (it cannot move on before thread 0 frees the
+        // stage, after the barriers below): one poll, which succeeds at once,
+        // gives every thread its own acquire of the landed bytes and slot.
+        if (ct != 0) ptx::mbar_try_wait(r.full(s), cur.parity);
+        // Every consumer thread reads the origin slot before the next barrier;
+        // consumer thread 0 frees the stage only after it, so no thread can
+        // see the slot refilled for a later box.
+        int32_t c[R];
+        landed_origin<R>(a, r, s, cur, c);
         if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
         const int lk = MODE == kStore ? (origin_error<R>(a, c) ? kLoadRefused : kLoadEngine) : load_kind<R>(a, c);
         const bool tload = lk == kLoadThreads;  // arrived with no bytes: the consumer threads load it
@@ -1200,6 +1230,12 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
         if (lk == kLoadRefused) kind = kStoreNothing;
         else if (MODE == kLoad) kind = wide ? kStorePlain : kStoreTensor;
         else kind = store_kind<R>(a, c);
+        // Consumer thread 0 may free the stage within this iteration (a box
+        // with nothing to store, or no store group allowed to stay in flight):
+        // then every thread must have read the origin slot first.  The paths
+        // that meet at a barrier below already ensure it.
+        if (a.coords && !tload && !ADD && kind != kStorePlain && (kind == kStoreNothing || a.store_lag == 0))
+            ptx::named_barrier_sync(1, CT);
         if (tload) {
             thread_load_box<R>(a, c, r.stage(s), ct, CT);
             if (kind == kStoreTensor) ptx::fence_proxy_async_smem();  // each writer, before the engine reads
