@@ -1201,23 +1201,20 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
     bool failed = false;
     for (; k < count; ++k, cur.advance(a, S)) {
         const uint32_t s = cur.stage;
-        // Consumer thread 0 alone polls the stage's barrier; the others wait at
-        // the named barrier, which takes no issue slots, and learn its outcome
-        // through the barrier's OR.
-        const bool ok = ct != 0 || wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
-        if (ptx::named_barrier_or(1, CT, !ok)) {
+        const bool ok = wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns);
+        if (!__all_sync(0xffffffffu, ok)) {
+            failed = true;
+        }
+        // Every consumer thread reads the origin slot before the barrier
+        // below; consumer thread 0 frees the stage only after that barrier, so
+        // no thread can see the slot refilled for a later box.
+        int32_t c[R];
+        landed_origin<R>(a, r, s, cur, c);
+        // every consumer warp must agree before any of them leaves the loop
+        if (ptx::named_barrier_or(1, CT, failed)) {
             failed = true;
             break;
         }
-        // The phase is complete (it cannot move on before thread 0 frees the
-        // stage, after the barriers below): one poll, which succeeds at once,
-        // gives every thread its own acquire of the landed bytes and slot.
-        if (ct != 0) ptx::mbar_try_wait(r.full(s), cur.parity);
-        // Every consumer thread reads the origin slot before the next barrier;
-        // consumer thread 0 frees the stage only after it, so no thread can
-        // see the slot refilled for a later box.
-        int32_t c[R];
-        landed_origin<R>(a, r, s, cur, c);
         if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
         const int lk = MODE == kStore ? (origin_error<R>(a, c) ? kLoadRefused : kLoadEngine) : load_kind<R>(a, c);
         const bool tload = lk == kLoadThreads;  // arrived with no bytes: the consumer threads load it
@@ -1230,12 +1227,6 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
         if (lk == kLoadRefused) kind = kStoreNothing;
         else if (MODE == kLoad) kind = wide ? kStorePlain : kStoreTensor;
         else kind = store_kind<R>(a, c);
-        // Consumer thread 0 may free the stage within this iteration (a box
-        // with nothing to store, or no store group allowed to stay in flight):
-        // then every thread must have read the origin slot first.  The paths
-        // that meet at a barrier below already ensure it.
-        if (a.coords && !tload && !ADD && kind != kStorePlain && (kind == kStoreNothing || a.store_lag == 0))
-            ptx::named_barrier_sync(1, CT);
         if (tload) {
             thread_load_box<R>(a, c, r.stage(s), ct, CT);
             if (kind == kStoreTensor) ptx::fence_proxy_async_smem();  // each writer, before the engine reads
