@@ -1162,7 +1162,10 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
 //         round-to-nearest fp32.  Two consumer warps.
 //   !ADD  gathers, stores and round trips over a coordinate list: four
 //         consumer warps.
-template <int MODE, int R, bool ADD>
+//   LISTED  launched with a coordinate list; false (the fp32 update over the
+//         tile grid) compiles the listed-box paths out: grid origins are
+//         always on the 16-byte grid and never refused.
+template <int MODE, int R, bool ADD, bool LISTED>
 __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumerThreads), ADD ? 1 : (MODE == kLoad ? 3 : 4))
     tile_wide_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
                      const __grid_constant__ CUtensorMap wide_map, const PipeArgs a, float addend)
@@ -1183,7 +1186,7 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
 
     const uint32_t count = my_tile_count(a);
     if (warp == 0) {
-        if (threadIdx.x == 0) producer_loop<MODE, R, true>(a, src_map, wide_map, r, count);
+        if (threadIdx.x == 0) producer_loop<MODE, R, LISTED>(a, src_map, wide_map, r, count);
         return;
     }
 
@@ -1216,7 +1219,9 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
             break;
         }
         if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
-        const int lk = MODE == kStore ? (origin_error<R>(a, c) ? kLoadRefused : kLoadEngine) : load_kind<R>(a, c);
+        const int lk = !LISTED          ? kLoadEngine
+                       : MODE == kStore ? (origin_error<R>(a, c) ? kLoadRefused : kLoadEngine)
+                                        : load_kind<R>(a, c);
         const bool tload = lk == kLoadThreads;  // arrived with no bytes: the consumer threads load it
         const bool wide = lk == kLoadWide;      // the wider image from the origin rounded down to the grid
         // How the box leaves.  Gathers: kStoreTensor = one bulk store of the
@@ -1266,6 +1271,8 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
         if (kind == kStorePlain) {
             if (MODE == kLoad)
                 pack_from_wide<R>(a, c, r.stage(s), a.packed + static_cast<size_t>(cur.t) * a.box_bytes, ct, CT);
+            else if (!LISTED)  // tile-grid origins sit on the 16-byte grid
+                plain_store_grid_box<R>(a, c, r.stage(s), ct, CT);
             else
                 plain_store_box<R>(a, c, r.stage(s), wide ? kFromWide : kFromImage, ct, CT);
             ptx::named_barrier_sync(1, CT);  // every reader is done with the stage
@@ -1331,15 +1338,15 @@ KernelFn grid_kernel(uint32_t rank, bool drain)
     return drain ? kernel_for_rank<MODE, false>(rank) : kernel_for_rank<MODE, true>(rank);
 }
 
-template <int MODE, bool ADD>
+template <int MODE, bool ADD, bool LISTED>
 WideKernelFn wide_kernel_for_rank(uint32_t rank)
 {
     switch (rank) {
-    case 1: return tile_wide_kernel<MODE, 1, ADD>;
-    case 2: return tile_wide_kernel<MODE, 2, ADD>;
-    case 3: return tile_wide_kernel<MODE, 3, ADD>;
-    case 4: return tile_wide_kernel<MODE, 4, ADD>;
-    default: return tile_wide_kernel<MODE, 5, ADD>;
+    case 1: return tile_wide_kernel<MODE, 1, ADD, LISTED>;
+    case 2: return tile_wide_kernel<MODE, 2, ADD, LISTED>;
+    case 3: return tile_wide_kernel<MODE, 3, ADD, LISTED>;
+    case 4: return tile_wide_kernel<MODE, 4, ADD, LISTED>;
+    default: return tile_wide_kernel<MODE, 5, ADD, LISTED>;
     }
 }
 
@@ -1527,8 +1534,10 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
                        (consumer == ATB_CONSUMER_DRAIN || (consumer == ATB_CONSUMER_AUTO && stage_b >= kDrainStageBytes));
     WideKernelFn wide_fn = nullptr;
     KernelFn grid_fn = nullptr;
-    if (MODE == kRoundtripAddF32) wide_fn = wide_kernel_for_rank<kRoundtrip, true>(rank);
-    else if (wide) wide_fn = wide_kernel_for_rank<kBase, false>(rank);
+    if (MODE == kRoundtripAddF32)
+        wide_fn = coords ? wide_kernel_for_rank<kRoundtrip, true, true>(rank)
+                         : wide_kernel_for_rank<kRoundtrip, true, false>(rank);
+    else if (wide) wide_fn = wide_kernel_for_rank<kBase, false, true>(rank);
     else grid_fn = grid_kernel<kBase>(rank, drain);
     const void* fn = wide ? reinterpret_cast<const void*>(wide_fn) : reinterpret_cast<const void*>(grid_fn);
     const uint32_t threads = MODE == kRoundtripAddF32 ? 32 + kUpdateConsumerThreads
