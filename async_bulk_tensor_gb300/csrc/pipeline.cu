@@ -231,6 +231,12 @@ struct BoxCursor {
             stage = 0;
             parity ^= 1u;
         }
+        step(a);
+    }
+
+    // To the next box: its index and tile coordinates only.
+    __device__ __forceinline__ void step(const PipeArgs& a)
+    {
         t += a.contiguous ? 1u : gridDim.x;
         uint32_t carry = 0;
 #pragma unroll
@@ -795,6 +801,30 @@ struct Ring {
     __device__ volatile uint32_t* abort_flag() const { return &ctl->abort; }
 };
 
+// A ring stage and its two barriers, stepped round the ring by additions:
+// the shared addresses of the current stage, of its full and empty barriers,
+// its index and the parity of its current use.
+struct StageWalk {
+    uint32_t stage, full, empty, s = 0, parity = 0;
+
+    __device__ __forceinline__ explicit StageWalk(const Ring& r) : stage(r.base), full(r.full0), empty(r.empty0) {}
+
+    __device__ __forceinline__ void next(const Ring& r)
+    {
+        if (++s == r.stages) {
+            s = 0;
+            parity ^= 1u;
+            stage = r.base;
+            full = r.full0;
+            empty = r.empty0;
+        } else {
+            stage += r.stage_bytes;
+            full += 8;
+            empty += 8;
+        }
+    }
+};
+
 __device__ __forceinline__ Ring ring_layout(const PipeArgs& a, uint8_t* smem_raw)
 {
     Ring r;
@@ -1009,45 +1039,91 @@ struct PendingStores {
     }
 };
 
+// The one-thread drain's producer: one thread walks the CTA's boxes of the
+// tile grid, waits until each box's stage is free, arms the stage's full
+// barrier with the box's byte count and issues the box's load (a tensor load,
+// or a 1-D bulk load of a packed image for stores).  Stage, barrier and
+// origin bookkeeping are additions only.
+template <int MODE, int R>
+__device__ __forceinline__ void grid_producer(const PipeArgs& a, const CUtensorMap& src_map, const Ring& r,
+                                              uint32_t count)
+{
+    const bool hint = (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
+    const uint64_t policy = hint ? ptx::policy_evict_first() : 0;
+    const bool check = (a.checks & ATB_CHECK_RING) != 0;
+    const uint32_t S = r.stages, bytes = a.box_bytes;
+    volatile uint32_t* issued = &r.ctl->issued;
+    BoxCursor<R> cur;
+    cur.init(a);
+    StageWalk w(r);
+    for (uint32_t k = 0; k < count; ++k, cur.step(a), w.next(r)) {
+        // the stage's previous use completed the empty phase of the other parity
+        if (k >= S && !wait_bounded(w.empty, w.parity ^ 1u, a.timeout_ns, r.abort_flag())) {
+            raise_abort(a, r, cur.t, kWhereProducerWait);
+            break;
+        }
+        if (check) {
+            ring_check_freed(a, r, w.s, k, cur.t);
+            *reinterpret_cast<volatile uint32_t*>(&r.ctl->filled[w.s]) = k + 1u;  // published by the arrive
+        }
+        ptx::mbar_arrive_expect_tx(w.full, bytes);
+        if (MODE == kStore) {
+            ptx::bulk_load(w.stage, a.packed + static_cast<size_t>(cur.t) * bytes, bytes, w.full);
+        } else {
+            int32_t c[R];
+            cur.grid_origin(a, c);
+            if (hint) ptx::tma_load_hint<R>(w.stage, &src_map, c, w.full, policy);
+            else ptx::tma_load<R>(w.stage, &src_map, c, w.full);
+        }
+        *issued = k + 1;
+    }
+    *reinterpret_cast<volatile uint32_t*>(&r.ctl->producer_done) = 1;
+}
+
 // One consumer thread drains every box of the tile grid with one engine copy:
 // a 1-D bulk store of the image into the packed buffer (gathers), or a tensor
 // store into the destination (round trips and stores whose destination holds
 // the whole grid and whose rows end on 16-byte boundaries).  Every box opens a
-// bulk group, so after committing box k the thread waits until at most `lag`
-// groups still read their stages and frees the stage of box k - lag.
-template <int MODE, int R>
-__device__ void drain_loop(const PipeArgs& a, const CUtensorMap& dst_map, const Ring& r, uint32_t count)
+// bulk group, so after committing box k the thread waits until at most L
+// groups still read their stages and frees the stage of box k - L.  L is the
+// launch's store lag, fixed at compile time for the lags up to 2 (LAG < 0:
+// read from the launch).
+template <int MODE, int R, int LAG>
+__device__ __forceinline__ void grid_drain(const PipeArgs& a, const CUtensorMap& dst_map, const Ring& r,
+                                           uint32_t count)
 {
-    const uint32_t S = r.stages, L = a.store_lag;
+    const uint32_t S = r.stages, L = LAG >= 0 ? static_cast<uint32_t>(LAG) : a.store_lag;
+    const bool check = (a.checks & ATB_CHECK_RING) != 0;
     const bool store_hint = (a.l2_hints & (ATB_HINT_STORE_EVICT_FIRST | ATB_HINT_STORE_EVICT_LAST)) != 0;
     const uint64_t store_policy = !store_hint ? 0
                                   : (a.l2_hints & ATB_HINT_STORE_EVICT_FIRST) ? ptx::policy_evict_first()
                                                                                : ptx::policy_evict_last();
     BoxCursor<R> cur;
     cur.init(a);
+    StageWalk w(r);
     uint32_t k = 0;
     bool failed = false;
-    for (; k < count; ++k, cur.advance(a, S)) {
-        const uint32_t s = cur.stage;
-        if (!wait_bounded(r.full(s), cur.parity, a.timeout_ns, r.abort_flag(), a.suspend_ns)) {
+    for (; k < count; ++k, cur.step(a), w.next(r)) {
+        if (!wait_bounded(w.full, w.parity, a.timeout_ns, r.abort_flag())) {
             failed = true;
             break;
         }
-        ring_check_filled(a, r, s, k, cur.t);
+        if (check) ring_check_filled(a, r, w.s, k, cur.t);
         ptx::fence_proxy_async_smem();
         if (MODE == kLoad) {
-            ptx::bulk_store(a.packed + static_cast<size_t>(cur.t) * a.box_bytes, r.stage(s), a.box_bytes);
+            ptx::bulk_store(a.packed + static_cast<size_t>(cur.t) * a.box_bytes, w.stage, a.box_bytes);
         } else {
             int32_t c[R];
             cur.grid_origin(a, c);
-            if (store_hint) ptx::tma_store_hint<R>(&dst_map, c, r.stage(s), store_policy);
-            else ptx::tma_store<R>(&dst_map, c, r.stage(s));
+            if (store_hint) ptx::tma_store_hint<R>(&dst_map, c, w.stage, store_policy);
+            else ptx::tma_store<R>(&dst_map, c, w.stage);
         }
         ptx::bulk_commit();
         if (k >= L) {  // the group of box k - L has finished reading its stage
-            ptx::bulk_wait_read_le(L);
-            const uint32_t sf = s >= L ? s - L : s + S - L;
-            ring_note_freed(a, r, sf, k - L);
+            if (LAG >= 0) ptx::bulk_wait_read<(LAG >= 0 ? LAG : 0)>();
+            else ptx::bulk_wait_read_le(L);
+            const uint32_t sf = w.s >= L ? w.s - L : w.s + S - L;
+            if (check) ring_note_freed(a, r, sf, k - L);
             ptx::mbar_arrive(r.empty(sf));
         }
     }
@@ -1057,8 +1133,9 @@ __device__ void drain_loop(const PipeArgs& a, const CUtensorMap& dst_map, const 
 
 // The tile-grid pipeline, 64 threads: warp 0 lane 0 produces, warp 1
 // consumes.
-//   GENERAL = false  every box is drained by one engine copy (drain_loop):
-//                    lane 0 of warp 1 is the whole consumer.
+//   GENERAL = false  every box is drained by one engine copy: thread 0 is
+//                    the producer (grid_producer) and thread 32 the whole
+//                    consumer (grid_drain).
 //   GENERAL = true   warp 1 follows every box; lane 0 issues the engine's
 //                    drain copies, and boxes that miss the destination or
 //                    cross the end of a row whose byte length is not a
@@ -1087,12 +1164,21 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
 
     const uint32_t count = my_tile_count(a);
 
-    if (warp == 0) {
-        if (lane == 0) producer_loop<MODE, R, false>(a, src_map, src_map, r, count);
+    if (!GENERAL) {
+        if (threadIdx.x == 0) {
+            grid_producer<MODE, R>(a, src_map, r, count);
+        } else if (threadIdx.x == 32) {
+            switch (a.store_lag) {
+            case 0: grid_drain<MODE, R, 0>(a, dst_map, r, count); break;
+            case 1: grid_drain<MODE, R, 1>(a, dst_map, r, count); break;
+            case 2: grid_drain<MODE, R, 2>(a, dst_map, r, count); break;
+            default: grid_drain<MODE, R, -1>(a, dst_map, r, count); break;
+            }
+        }
         return;
     }
-    if (!GENERAL) {
-        if (lane == 0) drain_loop<MODE, R>(a, dst_map, r, count);
+    if (warp == 0) {
+        if (lane == 0) producer_loop<MODE, R, false>(a, src_map, src_map, r, count);
         return;
     }
 
@@ -1492,7 +1578,6 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     DeviceInfo dev;
     atb_status st = current_device(&dev);
     if (st != ATB_OK) return st;
-    // a tile-grid launch with 16 KiB stages and no shape given: six stages, one CTA per SM, one store group
     // listed boxes off the 16-byte grid load the wider image into their stage
     const bool wide_loads = coords && MODE != kStore && shape->wide_box0;
     const uint32_t stage_b = stage_bytes_for(shape, wide_loads);
@@ -1529,9 +1614,12 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         if (MODE == kRoundtrip)
             for (uint32_t d = 0; d < rank; ++d) plain = plain || dst->dims[d] < src->dims[d];
     }
+    // The drain's producer neither prefetches nor suspends its polls: launches
+    // asking for either take the warp consumer.
     const uint32_t consumer = cfg ? cfg->consumer : ATB_CONSUMER_AUTO;
-    const bool drain = !wide && !plain &&
-                       (consumer == ATB_CONSUMER_DRAIN || (consumer == ATB_CONSUMER_AUTO && stage_b >= kDrainStageBytes));
+    const bool drain_fits = !wide && !plain && !(cfg && (cfg->prefetch_boxes || cfg->poll_suspend_ns));
+    const bool drain = drain_fits && (consumer == ATB_CONSUMER_DRAIN ||
+                                      (consumer == ATB_CONSUMER_AUTO && stage_b >= kDrainStageBytes));
     WideKernelFn wide_fn = nullptr;
     KernelFn grid_fn = nullptr;
     if (MODE == kRoundtripAddF32)

@@ -235,8 +235,8 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=device)
 
     w = datagen.C5A if args.box == "64x256" else datagen.C5B
-    launch = dict(stages=args.stages, ctas_per_sm=args.ctas_per_sm, poll_suspend_ns=args.poll_suspend_ns,
-                  consumer=args.consumer)
+    launch = dict(stages=args.stages, ctas_per_sm=args.ctas_per_sm, store_groups=args.store_groups,
+                  poll_suspend_ns=args.poll_suspend_ns, consumer=args.consumer)
     src_h = datagen.storage(w)
     nbytes = w.storage_bytes
     src = torch.from_numpy(src_h).to(device)
@@ -280,7 +280,7 @@ def run_gpu(args):
         "box": args.box, "swizzle": w.swizzle, "tiles_per_step": tiles,
         "stages": args.stages or "library default (3)",
         "ctas_per_sm": args.ctas_per_sm or "library default (96 KiB of stages per SM)",
-        "store_groups": "library default (2)", "launch": "programmatic dependent launch",
+        "store_groups": args.store_groups or "library default (2)", "launch": "programmatic dependent launch",
         "consumer": ("library default (warp consumer below 32 KiB stages, one-thread drain from 32 KiB)"
                      if args.consumer == "auto" else args.consumer),
         "parallelism": f"replicas x{world}",
@@ -723,6 +723,7 @@ def main(argv=None):
     p.add_argument("--box", choices=["64x256", "128x64"], default="128x64")
     p.add_argument("--stages", type=int, default=0, help="0 = library default")
     p.add_argument("--ctas-per-sm", type=int, default=0, help="0 = library default")
+    p.add_argument("--store-groups", type=int, default=0, help="0 = library default")
     p.add_argument("--poll-suspend-ns", type=int, default=0, help="mbarrier poll suspend hint (0 = default)")
     p.add_argument("--consumer", choices=["auto", "drain", "warp"], default="auto",
                    help="tile-grid consumer (auto = the library's choice)")

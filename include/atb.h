@@ -178,7 +178,8 @@ typedef struct {
  * atb_launch.consumer, for launches over the tile grid whose every box leaves
  * through one engine copy (gathers; stores and round trips whose destination
  * holds the whole grid and whose rows end on 16-byte boundaries).  Other
- * launches ignore it.
+ * launches ignore it, and launches with prefetch_boxes or poll_suspend_ns set
+ * always take the warp consumer.
  *   ATB_CONSUMER_AUTO   the library's choice: the warp consumer for stages
  *                       below 32 KiB, the one-thread drain from 32 KiB up
  *                       (the faster of the two for each size on GB300)
