@@ -72,6 +72,7 @@ struct PipeArgs {
     uint32_t stage_bytes;
     uint32_t stages;
     uint32_t store_lag;     // groups left reading after each commit
+    uint32_t early_release; // one-thread drain: free a stage before the next store
     uint32_t contiguous;    // 1: CTA b takes a contiguous run of boxes
     uint32_t swizzle_bits;  // 0 none, 1 32B, 2 64B, 3 128B
     uint32_t dst_ragged_x;  // destination rows end inside a 16-byte chunk
@@ -247,6 +248,51 @@ struct BoxCursor {
         }
         g[R - 1] += dg[R - 1] + carry;
     }
+};
+
+// The origin of a CTA's current box of the tile grid, stepped by additions
+// only: the step between consecutive boxes (gridDim.x boxes, or one for
+// contiguous runs) is kept per dimension in elements, and every coordinate
+// but the outermost wraps at most once per step.  The host runs this walk only
+// where every grid extent but the outermost is at most 2^31 elements, so no
+// sum overflows.  INDEX = true also keeps the box's index.
+template <int R, bool INDEX>
+struct GridWalk {
+    uint32_t c[R];   // origin, elements
+    uint32_t dc[R];  // the step, per dimension, in elements
+    uint32_t t = 0;  // index in the grid (INDEX)
+
+    __device__ __forceinline__ void init(const PipeArgs& a)
+    {
+        const uint32_t t0 = tile_of(a, 0);
+        if (INDEX) t = t0;
+        uint32_t rest = t0, rstep = a.contiguous ? 1u : gridDim.x;
+#pragma unroll
+        for (int d = 0; d < R - 1; ++d) {
+            c[d] = rest % a.grid[d] * a.box[d];
+            rest /= a.grid[d];
+            dc[d] = rstep % a.grid[d] * a.box[d];
+            rstep /= a.grid[d];
+        }
+        c[R - 1] = rest * a.box[R - 1];
+        dc[R - 1] = rstep * a.box[R - 1];
+    }
+
+    __device__ __forceinline__ void step(const PipeArgs& a)
+    {
+        if (INDEX) t += a.contiguous ? 1u : gridDim.x;
+        bool carry = false;
+#pragma unroll
+        for (int d = 0; d < R - 1; ++d) {
+            c[d] += dc[d] + (carry ? a.box[d] : 0u);
+            const uint32_t extent = a.grid[d] * a.box[d];
+            carry = c[d] >= extent;
+            if (carry) c[d] -= extent;
+        }
+        c[R - 1] += dc[R - 1] + (carry ? a.box[R - 1] : 0u);
+    }
+
+    __device__ __forceinline__ const int32_t* origin() const { return reinterpret_cast<const int32_t*>(c); }
 };
 
 // A listed origin the engine must not be given: beyond +-2^30 along any
@@ -801,26 +847,17 @@ struct Ring {
     __device__ volatile uint32_t* abort_flag() const { return &ctl->abort; }
 };
 
-// A ring stage and its two barriers, stepped round the ring by additions:
-// the shared addresses of the current stage, of its full and empty barriers,
-// its index and the parity of its current use.
+// A CTA's walk round the ring: the current stage's index and the parity of
+// its current use; the stage's and its barriers' shared addresses follow from
+// the index.
 struct StageWalk {
-    uint32_t stage, full, empty, s = 0, parity = 0;
-
-    __device__ __forceinline__ explicit StageWalk(const Ring& r) : stage(r.base), full(r.full0), empty(r.empty0) {}
+    uint32_t s = 0, parity = 0;
 
     __device__ __forceinline__ void next(const Ring& r)
     {
         if (++s == r.stages) {
             s = 0;
             parity ^= 1u;
-            stage = r.base;
-            full = r.full0;
-            empty = r.empty0;
-        } else {
-            stage += r.stage_bytes;
-            full += 8;
-            empty += 8;
         }
     }
 };
@@ -1042,39 +1079,35 @@ struct PendingStores {
 // The one-thread drain's producer: one thread walks the CTA's boxes of the
 // tile grid, waits until each box's stage is free, arms the stage's full
 // barrier with the box's byte count and issues the box's load (a tensor load,
-// or a 1-D bulk load of a packed image for stores).  Stage, barrier and
-// origin bookkeeping are additions only.
-template <int MODE, int R>
+// or a 1-D bulk load of a packed image for stores).  OPTS = false compiles the
+// ring check and the L2 hint out.
+template <int MODE, int R, bool OPTS>
 __device__ __forceinline__ void grid_producer(const PipeArgs& a, const CUtensorMap& src_map, const Ring& r,
                                               uint32_t count)
 {
-    const bool hint = (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
+    const bool hint = OPTS && (a.l2_hints & ATB_HINT_LOAD_EVICT_FIRST) != 0;
     const uint64_t policy = hint ? ptx::policy_evict_first() : 0;
-    const bool check = (a.checks & ATB_CHECK_RING) != 0;
+    const bool check = OPTS && (a.checks & ATB_CHECK_RING) != 0;
     const uint32_t S = r.stages, bytes = a.box_bytes;
     volatile uint32_t* issued = &r.ctl->issued;
-    BoxCursor<R> cur;
-    cur.init(a);
-    StageWalk w(r);
-    for (uint32_t k = 0; k < count; ++k, cur.step(a), w.next(r)) {
+    GridWalk<R, MODE == kStore> g;
+    g.init(a);
+    StageWalk w;
+    for (uint32_t k = 0; k < count; ++k, g.step(a), w.next(r)) {
         // the stage's previous use completed the empty phase of the other parity
-        if (k >= S && !wait_bounded(w.empty, w.parity ^ 1u, a.timeout_ns, r.abort_flag())) {
-            raise_abort(a, r, cur.t, kWhereProducerWait);
+        if (k >= S && !wait_bounded(r.empty(w.s), w.parity ^ 1u, a.timeout_ns, r.abort_flag())) {
+            raise_abort(a, r, tile_of(a, k), kWhereProducerWait);
             break;
         }
         if (check) {
-            ring_check_freed(a, r, w.s, k, cur.t);
+            ring_check_freed(a, r, w.s, k, tile_of(a, k));
             *reinterpret_cast<volatile uint32_t*>(&r.ctl->filled[w.s]) = k + 1u;  // published by the arrive
         }
-        ptx::mbar_arrive_expect_tx(w.full, bytes);
-        if (MODE == kStore) {
-            ptx::bulk_load(w.stage, a.packed + static_cast<size_t>(cur.t) * bytes, bytes, w.full);
-        } else {
-            int32_t c[R];
-            cur.grid_origin(a, c);
-            if (hint) ptx::tma_load_hint<R>(w.stage, &src_map, c, w.full, policy);
-            else ptx::tma_load<R>(w.stage, &src_map, c, w.full);
-        }
+        const uint32_t full = r.full(w.s), stage = r.stage(w.s);
+        ptx::mbar_arrive_expect_tx(full, bytes);
+        if (MODE == kStore) ptx::bulk_load(stage, a.packed + static_cast<size_t>(g.t) * bytes, bytes, full);
+        else if (hint) ptx::tma_load_hint<R>(stage, &src_map, g.origin(), full, policy);
+        else ptx::tma_load<R>(stage, &src_map, g.origin(), full);
         *issued = k + 1;
     }
     *reinterpret_cast<volatile uint32_t*>(&r.ctl->producer_done) = 1;
@@ -1084,48 +1117,62 @@ __device__ __forceinline__ void grid_producer(const PipeArgs& a, const CUtensorM
 // a 1-D bulk store of the image into the packed buffer (gathers), or a tensor
 // store into the destination (round trips and stores whose destination holds
 // the whole grid and whose rows end on 16-byte boundaries).  Every box opens a
-// bulk group, so after committing box k the thread waits until at most L
-// groups still read their stages and frees the stage of box k - L.  L is the
-// launch's store lag, fixed at compile time for the lags up to 2 (LAG < 0:
-// read from the launch).
-template <int MODE, int R, int LAG>
+// bulk group and at most L + 1 groups read their stages at once (L, the
+// launch's store lag, is fixed at compile time up to 2; LAG < 0 reads it from
+// the launch).  A stage is released once its group has finished reading:
+//   EARLY = false  after committing box k the thread waits until at most L
+//                  groups still read and frees the stage of box k - L;
+//   EARLY = true   before storing box k the thread waits until at most L
+//                  groups still read and frees the stage of box k - L - 1,
+//                  so that the load into that stage is issued ahead of the
+//                  store of box k (needs L + 1 < stages).  The thread first
+//                  pauses for about kEarlyReleasePauseNs after each box lands.
+// Measured on GB300 (512 MiB fp16 round trip, 16 KiB boxes, seven stages, one
+// CTA per SM, three store groups): early release with the pause sustained
+// 6,786-6,799 GB/s, early release without it 6,694-6,716, and the late order
+// 6,627-6,633; a pause of the same length in the producer did not help.
+constexpr unsigned kEarlyReleasePauseNs = 64;
+
+template <int MODE, int R, int LAG, bool EARLY, bool OPTS>
 __device__ __forceinline__ void grid_drain(const PipeArgs& a, const CUtensorMap& dst_map, const Ring& r,
                                            uint32_t count)
 {
     const uint32_t S = r.stages, L = LAG >= 0 ? static_cast<uint32_t>(LAG) : a.store_lag;
-    const bool check = (a.checks & ATB_CHECK_RING) != 0;
-    const bool store_hint = (a.l2_hints & (ATB_HINT_STORE_EVICT_FIRST | ATB_HINT_STORE_EVICT_LAST)) != 0;
+    const uint32_t lag = EARLY ? L + 1 : L;  // boxes between a box and the release of its stage
+    const bool check = OPTS && (a.checks & ATB_CHECK_RING) != 0;
+    const bool store_hint =
+        OPTS && (a.l2_hints & (ATB_HINT_STORE_EVICT_FIRST | ATB_HINT_STORE_EVICT_LAST)) != 0;
     const uint64_t store_policy = !store_hint ? 0
                                   : (a.l2_hints & ATB_HINT_STORE_EVICT_FIRST) ? ptx::policy_evict_first()
                                                                                : ptx::policy_evict_last();
-    BoxCursor<R> cur;
-    cur.init(a);
-    StageWalk w(r);
+    auto release = [&](const StageWalk& w, uint32_t k) {  // the stage of box k - lag
+        if (LAG >= 0) ptx::bulk_wait_read<(LAG >= 0 ? LAG : 0)>();
+        else ptx::bulk_wait_read_le(L);
+        uint32_t sf = w.s + S - lag;  // lag < S
+        if (sf >= S) sf -= S;
+        if (check) ring_note_freed(a, r, sf, k - lag);
+        ptx::mbar_arrive(r.empty(sf));
+    };
+    GridWalk<R, MODE == kLoad> g;
+    g.init(a);
+    StageWalk w;
     uint32_t k = 0;
     bool failed = false;
-    for (; k < count; ++k, cur.step(a), w.next(r)) {
-        if (!wait_bounded(w.full, w.parity, a.timeout_ns, r.abort_flag())) {
+    for (; k < count; ++k, g.step(a), w.next(r)) {
+        if (!wait_bounded(r.full(w.s), w.parity, a.timeout_ns, r.abort_flag())) {
             failed = true;
             break;
         }
-        if (check) ring_check_filled(a, r, w.s, k, cur.t);
+        if (EARLY) __nanosleep(kEarlyReleasePauseNs);
+        if (check) ring_check_filled(a, r, w.s, k, tile_of(a, k));
+        if (EARLY && k + 1 > lag) release(w, k);
         ptx::fence_proxy_async_smem();
-        if (MODE == kLoad) {
-            ptx::bulk_store(a.packed + static_cast<size_t>(cur.t) * a.box_bytes, w.stage, a.box_bytes);
-        } else {
-            int32_t c[R];
-            cur.grid_origin(a, c);
-            if (store_hint) ptx::tma_store_hint<R>(&dst_map, c, w.stage, store_policy);
-            else ptx::tma_store<R>(&dst_map, c, w.stage);
-        }
+        const uint32_t stage = r.stage(w.s);
+        if (MODE == kLoad) ptx::bulk_store(a.packed + static_cast<size_t>(g.t) * a.box_bytes, stage, a.box_bytes);
+        else if (store_hint) ptx::tma_store_hint<R>(&dst_map, g.origin(), stage, store_policy);
+        else ptx::tma_store<R>(&dst_map, g.origin(), stage);
         ptx::bulk_commit();
-        if (k >= L) {  // the group of box k - L has finished reading its stage
-            if (LAG >= 0) ptx::bulk_wait_read<(LAG >= 0 ? LAG : 0)>();
-            else ptx::bulk_wait_read_le(L);
-            const uint32_t sf = w.s >= L ? w.s - L : w.s + S - L;
-            if (check) ring_note_freed(a, r, sf, k - L);
-            ptx::mbar_arrive(r.empty(sf));
-        }
+        if (!EARLY && k + 1 > lag) release(w, k);
     }
     ptx::bulk_wait_all();
     if (failed) drain_after_failure(a, r, k);
@@ -1133,15 +1180,20 @@ __device__ __forceinline__ void grid_drain(const PipeArgs& a, const CUtensorMap&
 
 // The tile-grid pipeline, 64 threads: warp 0 lane 0 produces, warp 1
 // consumes.
-//   GENERAL = false  every box is drained by one engine copy: thread 0 is
-//                    the producer (grid_producer) and thread 32 the whole
-//                    consumer (grid_drain).
-//   GENERAL = true   warp 1 follows every box; lane 0 issues the engine's
-//                    drain copies, and boxes that miss the destination or
-//                    cross the end of a row whose byte length is not a
-//                    multiple of 16 are written by the warp with plain clipped
-//                    stores.
-template <int MODE, int R, bool GENERAL>
+//   kConsumerDrain      every box is drained by one engine copy: thread 0
+//                       is the producer (grid_producer) and thread 32 the
+//                       whole consumer (grid_drain);
+//   kConsumerDrainOpts  the same with the ring check and L2 hints compiled in;
+//   kConsumerWarp       warp 1 follows every box; lane 0 issues the engine's
+//                       drain copies, and boxes that miss the destination or
+//                       cross the end of a row whose byte length is not a
+//                       multiple of 16 are written by the warp with plain
+//                       clipped stores.
+constexpr int kConsumerWarp = 0;
+constexpr int kConsumerDrain = 1;
+constexpr int kConsumerDrainOpts = 2;
+
+template <int MODE, int R, int CONSUMER>
 __global__ void __launch_bounds__(kPipelineThreads, 1)
     tile_pipeline_kernel(const __grid_constant__ CUtensorMap src_map, const __grid_constant__ CUtensorMap dst_map,
                          const PipeArgs a)
@@ -1164,15 +1216,24 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
 
     const uint32_t count = my_tile_count(a);
 
-    if (!GENERAL) {
+    if (CONSUMER != kConsumerWarp) {
+        constexpr bool O = CONSUMER == kConsumerDrainOpts;
         if (threadIdx.x == 0) {
-            grid_producer<MODE, R>(a, src_map, r, count);
+            grid_producer<MODE, R, O>(a, src_map, r, count);
         } else if (threadIdx.x == 32) {
-            switch (a.store_lag) {
-            case 0: grid_drain<MODE, R, 0>(a, dst_map, r, count); break;
-            case 1: grid_drain<MODE, R, 1>(a, dst_map, r, count); break;
-            case 2: grid_drain<MODE, R, 2>(a, dst_map, r, count); break;
-            default: grid_drain<MODE, R, -1>(a, dst_map, r, count); break;
+            if (a.early_release) {
+                switch (a.store_lag) {
+                case 1: grid_drain<MODE, R, 1, true, O>(a, dst_map, r, count); break;
+                case 2: grid_drain<MODE, R, 2, true, O>(a, dst_map, r, count); break;
+                default: grid_drain<MODE, R, -1, true, O>(a, dst_map, r, count); break;
+                }
+            } else {
+                switch (a.store_lag) {
+                case 0: grid_drain<MODE, R, 0, false, O>(a, dst_map, r, count); break;
+                case 1: grid_drain<MODE, R, 1, false, O>(a, dst_map, r, count); break;
+                case 2: grid_drain<MODE, R, 2, false, O>(a, dst_map, r, count); break;
+                default: grid_drain<MODE, R, -1, false, O>(a, dst_map, r, count); break;
+                }
             }
         }
         return;
@@ -1404,24 +1465,23 @@ __global__ void wait_timeout_selftest_kernel(DeviceStatus* st, uint64_t timeout_
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const PipeArgs);
 using WideKernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PipeArgs, float);
 
-template <int MODE, bool GENERAL>
+template <int MODE, int CONSUMER>
 KernelFn kernel_for_rank(uint32_t rank)
 {
     switch (rank) {
-    case 1: return tile_pipeline_kernel<MODE, 1, GENERAL>;
-    case 2: return tile_pipeline_kernel<MODE, 2, GENERAL>;
-    case 3: return tile_pipeline_kernel<MODE, 3, GENERAL>;
-    case 4: return tile_pipeline_kernel<MODE, 4, GENERAL>;
-    default: return tile_pipeline_kernel<MODE, 5, GENERAL>;
+    case 1: return tile_pipeline_kernel<MODE, 1, CONSUMER>;
+    case 2: return tile_pipeline_kernel<MODE, 2, CONSUMER>;
+    case 3: return tile_pipeline_kernel<MODE, 3, CONSUMER>;
+    case 4: return tile_pipeline_kernel<MODE, 4, CONSUMER>;
+    default: return tile_pipeline_kernel<MODE, 5, CONSUMER>;
     }
 }
 
-// The tile-grid kernel for a launch: the one-thread drain, or the warp
-// consumer (which can also write boxes with plain clipped stores).
 template <int MODE>
-KernelFn grid_kernel(uint32_t rank, bool drain)
+KernelFn grid_kernel(uint32_t rank, bool drain, bool opts)
 {
-    return drain ? kernel_for_rank<MODE, false>(rank) : kernel_for_rank<MODE, true>(rank);
+    if (!drain) return kernel_for_rank<MODE, kConsumerWarp>(rank);
+    return opts ? kernel_for_rank<MODE, kConsumerDrainOpts>(rank) : kernel_for_rank<MODE, kConsumerDrain>(rank);
 }
 
 template <int MODE, bool ADD, bool LISTED>
@@ -1469,6 +1529,19 @@ constexpr uint32_t kDefaultStoreGroups = 2;
 constexpr uint64_t kStageBytesPerSm = 96u * 1024u;
 constexpr uint64_t kMaxDefaultCtasPerSm = 8;
 constexpr uint32_t kDrainStageBytes = 32u * 1024u;
+
+// The one-thread drain's own default ring for stages of 8 to 32 KiB, measured
+// on GB300 (16 KiB boxes of a 512 MiB fp16 round trip, one CTA per SM, rings
+// of 6 to 12 stages with every store-group count, stages released before or
+// after the next store): about 64 KiB of stages waiting for or holding landed
+// boxes plus 48 KiB of store groups in flight, one CTA per SM, each stage
+// freed before the next store is issued so that the load into it goes out
+// first.  Every ring with four stages on the load side and three to six
+// store groups sustained 6,786-6,796 GB/s; three or five load-side stages
+// fell to 6,190-6,240.
+constexpr uint32_t kDrainMinStageBytes = 8u * 1024u;
+constexpr uint32_t kDrainLoadSideBytes = 64u * 1024u;
+constexpr uint32_t kDrainStoreSideBytes = 48u * 1024u;
 
 uint32_t default_stages(const atb_tensor_map* m, const DeviceInfo& dev, bool wide_loads)
 {
@@ -1581,7 +1654,41 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     // listed boxes off the 16-byte grid load the wider image into their stage
     const bool wide_loads = coords && MODE != kStore && shape->wide_box0;
     const uint32_t stage_b = stage_bytes_for(shape, wide_loads);
-    const uint32_t stages = cfg && cfg->stages ? cfg->stages : default_stages(shape, dev, wide_loads);
+
+    // Launches over a coordinate list (whose boxes may start before the tensor
+    // or off the 16-byte grid along x) and the fp32 update run the kernel with
+    // several consumer warps; tile-grid launches run the 64-thread kernel.
+    constexpr int kBase = MODE == kRoundtripAddF32 ? kRoundtrip : MODE;
+    const bool wide = MODE == kRoundtripAddF32 || coords != nullptr;
+    // Tile grid: where every box leaves through one engine copy (no box misses
+    // the destination or crosses a ragged row end) either consumer serves.
+    // The library takes the one-thread drain for stages of 32 KiB and more,
+    // and for stages of 8 to 32 KiB when the caller leaves the ring's shape to
+    // it (the drain then runs its own deeper ring, one CTA per SM); the warp
+    // consumer otherwise (measured on GB300: each was the faster there).  The
+    // warp consumer, which can also write plain clipped stores, serves the
+    // rest.  The drain's producer neither prefetches nor suspends its polls:
+    // launches asking for either take the warp consumer, as do grids wider
+    // than 2^31 elements along a dimension below the outermost.
+    bool plain = false;
+    if (!wide && MODE != kLoad) {
+        plain = (dst->dims[0] * dst->esize) % 16 != 0;
+        if (MODE == kRoundtrip)
+            for (uint32_t d = 0; d < rank; ++d) plain = plain || dst->dims[d] < src->dims[d];
+    }
+    const uint32_t consumer = cfg ? cfg->consumer : ATB_CONSUMER_AUTO;
+    bool drain_fits = !wide && !plain && !(cfg && (cfg->prefetch_boxes || cfg->poll_suspend_ns));
+    for (uint32_t d = 0; d + 1 < rank; ++d)  // the drain's origin walk: extents of at most 2^31 elements
+        drain_fits = drain_fits && (shape->dims[d] + shape->box[d] - 1) / shape->box[d] * shape->box[d] <= (1ull << 31);
+    const bool shape_given = cfg && (cfg->stages || cfg->store_groups || cfg->ctas_per_sm);
+    const bool deep_fits = !shape_given && stage_b >= kDrainMinStageBytes && stage_b < kDrainStageBytes;
+    const bool drain = drain_fits && (consumer == ATB_CONSUMER_DRAIN ||
+                                      (consumer == ATB_CONSUMER_AUTO && (stage_b >= kDrainStageBytes || deep_fits)));
+    const bool deep = drain && deep_fits;
+    const uint32_t deep_groups = deep ? kDrainStoreSideBytes / stage_b : 0u;
+    const uint32_t stages = cfg && cfg->stages ? cfg->stages
+                            : deep             ? kDrainLoadSideBytes / stage_b + deep_groups
+                                               : default_stages(shape, dev, wide_loads);
     if (stages < 1 || stages > kMaxStages)
         return set_error(ATB_ERR_ARG, "stages = %u is outside 1..%u", stages, kMaxStages);
     const size_t smem = smem_bytes_for(shape, stages, wide_loads);
@@ -1597,36 +1704,13 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         if (st != ATB_OK) return st;
     }
 
-    // Launches over a coordinate list (whose boxes may start before the tensor
-    // or off the 16-byte grid along x) and the fp32 update run the kernel with
-    // several consumer warps; tile-grid launches run the 64-thread kernel.
-    constexpr int kBase = MODE == kRoundtripAddF32 ? kRoundtrip : MODE;
-    const bool wide = MODE == kRoundtripAddF32 || coords != nullptr;
-    // Tile grid: where every box leaves through one engine copy (no box misses
-    // the destination or crosses a ragged row end) either consumer serves; the
-    // library takes the one-thread drain for stages of 32 KiB and more and the
-    // warp consumer below (measured on GB300: each was the faster there, and
-    // the warp consumer's lead below 32 KiB held in every build measured).
-    // The warp consumer, which can also write plain clipped stores, otherwise.
-    bool plain = false;
-    if (!wide && MODE != kLoad) {
-        plain = (dst->dims[0] * dst->esize) % 16 != 0;
-        if (MODE == kRoundtrip)
-            for (uint32_t d = 0; d < rank; ++d) plain = plain || dst->dims[d] < src->dims[d];
-    }
-    // The drain's producer neither prefetches nor suspends its polls: launches
-    // asking for either take the warp consumer.
-    const uint32_t consumer = cfg ? cfg->consumer : ATB_CONSUMER_AUTO;
-    const bool drain_fits = !wide && !plain && !(cfg && (cfg->prefetch_boxes || cfg->poll_suspend_ns));
-    const bool drain = drain_fits && (consumer == ATB_CONSUMER_DRAIN ||
-                                      (consumer == ATB_CONSUMER_AUTO && stage_b >= kDrainStageBytes));
     WideKernelFn wide_fn = nullptr;
     KernelFn grid_fn = nullptr;
     if (MODE == kRoundtripAddF32)
         wide_fn = coords ? wide_kernel_for_rank<kRoundtrip, true, true>(rank)
                          : wide_kernel_for_rank<kRoundtrip, true, false>(rank);
     else if (wide) wide_fn = wide_kernel_for_rank<kBase, false, true>(rank);
-    else grid_fn = grid_kernel<kBase>(rank, drain);
+    else grid_fn = grid_kernel<kBase>(rank, drain, cfg && (cfg->checks || cfg->l2_hints));
     const void* fn = wide ? reinterpret_cast<const void*>(wide_fn) : reinterpret_cast<const void*>(grid_fn);
     const uint32_t threads = MODE == kRoundtripAddF32 ? 32 + kUpdateConsumerThreads
                              : wide                     ? kTransformThreads
@@ -1635,7 +1719,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     st = kernel_fit(fn, dev, threads, smem, &fit);
     if (st != ATB_OK) return st;
 
-    uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm : 0u;
+    uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm : deep ? 1u : 0u;
     if (!per_sm) {
         // sized on the box image: a wider stage for off-grid loads does not cut the CTA count
         uint64_t want = kStageBytesPerSm / (static_cast<uint64_t>(stages) * stage_bytes_for(shape));
@@ -1657,10 +1741,11 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.box_bytes = shape->box_bytes;
     a.stage_bytes = stage_b;
     a.stages = stages;
-    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : kDefaultStoreGroups;
+    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : deep ? deep_groups : kDefaultStoreGroups;
     if (groups > stages) groups = stages;
     if (groups > 8) groups = 8;
     a.store_lag = groups - 1;
+    a.early_release = deep && groups < stages ? 1u : 0u;
     a.contiguous = cfg && cfg->schedule == 1 ? 1u : 0u;
     a.l2_hints = cfg ? cfg->l2_hints : 0u;
     a.suspend_ns = cfg ? cfg->poll_suspend_ns : 0u;

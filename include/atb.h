@@ -157,12 +157,15 @@ typedef struct {
 
 /* Pipeline shape of one launch.  Zero fields take the library defaults. */
 typedef struct {
-    uint32_t stages;       /* shared-memory ring depth, 1..16 (0 = 3, or fewer if 3 do not fit) */
+    uint32_t stages;       /* shared-memory ring depth, 1..16 (0 = 3, or fewer if 3 do not fit;
+                              the drain's own ring: see atb_launch.consumer) */
     uint32_t ctas;         /* total CTAs; 0 = persistent grid of ctas_per_sm per SM */
-    uint32_t ctas_per_sm;  /* 0 = about 96 KiB of stages per SM (1..8), within what fits */
+    uint32_t ctas_per_sm;  /* 0 = about 96 KiB of stages per SM (1..8), within what fits;
+                              one for the drain's own ring */
     uint32_t schedule;     /* 0 = box t goes to CTA t mod G; 1 = CTA b takes a contiguous run */
     uint32_t store_groups; /* bulk-store groups allowed in flight at once, 1..8, clamped to
-                              `stages` (0 = 2); a stage is recycled as soon as
+                              `stages` (0 = the library's choice, 2 but for the
+                              drain's own ring); a stage is recycled as soon as
                               the group that stores from it has finished reading it */
     uint32_t l2_hints;     /* ATB_HINT_* bits: L2 eviction policy of the box loads and stores */
     uint32_t no_pdl;       /* 1 = launch without programmatic dependent launch (see below) */
@@ -180,9 +183,15 @@ typedef struct {
  * holds the whole grid and whose rows end on 16-byte boundaries).  Other
  * launches ignore it, and launches with prefetch_boxes or poll_suspend_ns set
  * always take the warp consumer.
- *   ATB_CONSUMER_AUTO   the library's choice: the warp consumer for stages
- *                       below 32 KiB, the one-thread drain from 32 KiB up
- *                       (the faster of the two for each size on GB300)
+ *   ATB_CONSUMER_AUTO   the library's choice: the one-thread drain for
+ *                       stages of 32 KiB and more, and for stages of 8 to
+ *                       32 KiB when the launch leaves stages, store_groups
+ *                       and ctas_per_sm at 0 (the drain then runs its own
+ *                       ring: about 64 KiB of stages for boxes being loaded
+ *                       or landed plus 48 KiB of store groups, one CTA per
+ *                       SM, each stage freed before the next store is
+ *                       issued); the warp consumer otherwise (the faster
+ *                       choice for each case on GB300)
  *   ATB_CONSUMER_DRAIN  one consumer thread per CTA waits for each stage and
  *                       issues its drain copy; fewest instructions per box
  *   ATB_CONSUMER_WARP   a consumer warp follows every box and its lane 0
