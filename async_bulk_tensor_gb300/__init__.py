@@ -85,7 +85,7 @@ class Launch(ctypes.Structure):
         ("prefetch_boxes", ctypes.c_uint32),
         ("checks", ctypes.c_uint32),
         ("consumer", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32 * 1),
+        ("release", ctypes.c_uint32),
     ]
 
 
@@ -102,6 +102,14 @@ class DeviceReport(ctypes.Structure):
     def as_dict(self):
         return {"code": self.code, "name": STATUS[self.code] if 0 <= self.code < len(STATUS) else "?",
                 "block": self.block, "tile": self.tile, "where": self.where, "errors": self.errors}
+
+
+class LaunchShape(ctypes.Structure):
+    """Mirror of ``atb_launch_shape``."""
+
+    _fields_ = [(name, ctypes.c_uint32) for name in ("consumer", "release", "stages", "store_groups",
+                                                     "ctas_per_sm", "ctas", "threads", "smem_bytes", "boxes")]
+    _fields_ += [("reserved", ctypes.c_uint32 * 3)]
 
 
 def _load():
@@ -127,6 +135,7 @@ def _load():
         "atb_init_device": (S, []),
         "atb_device_status": (S, [P, ctypes.POINTER(DeviceReport)]),
         "atb_status_block_allocated": (ctypes.c_int, []),
+        "atb_last_launch": (S, [ctypes.POINTER(LaunchShape)]),
         "atb_set_wait_timeout_ns": (None, [U64]),
         "atb_selftest_wait_timeout": (S, [U64, P]),
         "atb_tile_roundtrip_noalloc": (S, [MapP, MapP, P, U64, LaunchP, P, ctypes.POINTER(DeviceReport)]),
@@ -239,13 +248,15 @@ HINT_LOAD_EVICT_FIRST, HINT_STORE_EVICT_FIRST, HINT_STORE_EVICT_LAST = 1, 2, 4
 
 
 CONSUMERS = {"auto": 0, "drain": 1, "warp": 2}
+RELEASES = {"auto": 0, "after_store": 1, "before_store": 2}
 
 
 def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True,
-            poll_suspend_ns=0, prefetch_boxes=0, checks=0, consumer="auto") -> Launch:
+            poll_suspend_ns=0, prefetch_boxes=0, checks=0, consumer="auto", release="auto") -> Launch:
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
                   store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes, checks,
-                  CONSUMERS[consumer] if isinstance(consumer, str) else consumer)
+                  CONSUMERS[consumer] if isinstance(consumer, str) else consumer,
+                  RELEASES[release] if isinstance(release, str) else release)
 
 
 def version() -> int:
@@ -358,6 +369,17 @@ def tile_roundtrip_noalloc(src: TensorMap, dst: TensorMap, coords=None, n: int =
 
 def init_device():
     _check(lib.atb_init_device(), "atb_init_device")
+
+
+def last_launch() -> dict:
+    """``atb_last_launch``: the shape of this thread's most recent pipeline launch
+    (all zero when it launched nothing)."""
+    out = LaunchShape()
+    _check(lib.atb_last_launch(ctypes.byref(out)), "atb_last_launch")
+    d = {name: getattr(out, name) for name, _ in LaunchShape._fields_ if name != "reserved"}
+    d["consumer"] = {0: None, 1: "drain", 2: "warp", 3: "warps"}.get(d["consumer"], d["consumer"])
+    d["release"] = {0: None, 1: "after_store", 2: "before_store"}.get(d["release"], d["release"])
+    return d
 
 
 def status_block_allocated() -> int:

@@ -1602,6 +1602,9 @@ atb_status kernel_fit(const void* fn, const DeviceInfo& dev, uint32_t threads, s
 // the device's lazily allocated status block.
 // Launches one pipeline over boxes [first, first + count) of the list or grid
 // (count = UINT64_MAX: all of them).
+// The shape of this host thread's most recent pipeline launch (atb_last_launch).
+thread_local atb_launch_shape g_last_shape = {};
+
 template <int MODE>
 atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst, const int32_t* coords, uint64_t n,
                            void* packed, const atb_launch* cfg, cudaStream_t stream,
@@ -1609,6 +1612,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
                            uint64_t count = UINT64_MAX)
 {
     clear_error();
+    g_last_shape = atb_launch_shape{};
     const atb_tensor_map* shape = MODE == kStore ? dst : src;
     if ((MODE != kStore && !map_is_valid(src)) || (MODE != kLoad && !map_is_valid(dst)))
         return set_error(ATB_ERR_ARG, "tensor map is NULL or was not produced by atb_encode_tiled");
@@ -1627,6 +1631,8 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         return set_error(ATB_ERR_ARG, "unknown check bits 0x%x", cfg->checks & ~ATB_CHECK_RING);
     if (cfg && cfg->consumer > ATB_CONSUMER_WARP)
         return set_error(ATB_ERR_ARG, "unknown consumer %u", cfg->consumer);
+    if (cfg && cfg->release > ATB_RELEASE_BEFORE_STORE)
+        return set_error(ATB_ERR_ARG, "unknown release %u", cfg->release);
     if (MODE == kLoad || MODE == kStore) {
         if (!packed) return set_error(ATB_ERR_ARG, "packed buffer is NULL");
         if (reinterpret_cast<uintptr_t>(packed) % 16)
@@ -1696,6 +1702,15 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         return set_error(ATB_ERR_SMEM_BUDGET,
                          "%u stages of %u bytes need %zu bytes of shared memory; a block may have at most %d",
                          stages, stage_b, smem, dev.smem_optin);
+    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : deep ? deep_groups : kDefaultStoreGroups;
+    if (groups > stages) groups = stages;
+    if (groups > 8) groups = 8;
+    const uint32_t release = cfg ? cfg->release : ATB_RELEASE_AUTO;
+    if (drain && release == ATB_RELEASE_BEFORE_STORE && groups >= stages)
+        return set_error(ATB_ERR_ARG, "releasing before the next store needs store_groups (%u) < stages (%u)", groups,
+                         stages);
+    const bool early =
+        drain && groups < stages && (release == ATB_RELEASE_BEFORE_STORE || (release == ATB_RELEASE_AUTO && deep));
     if (n_tiles == 0) return ATB_OK;
 
     DeviceStatus* status = caller_status;
@@ -1741,11 +1756,8 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     a.box_bytes = shape->box_bytes;
     a.stage_bytes = stage_b;
     a.stages = stages;
-    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : deep ? deep_groups : kDefaultStoreGroups;
-    if (groups > stages) groups = stages;
-    if (groups > 8) groups = 8;
     a.store_lag = groups - 1;
-    a.early_release = deep && groups < stages ? 1u : 0u;
+    a.early_release = early ? 1u : 0u;
     a.contiguous = cfg && cfg->schedule == 1 ? 1u : 0u;
     a.l2_hints = cfg ? cfg->l2_hints : 0u;
     a.suspend_ns = cfg ? cfg->poll_suspend_ns : 0u;
@@ -1807,6 +1819,16 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     else
         e = cudaLaunchKernelEx(&lc, grid_fn, src_map, dst_map, a);
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
+    atb_launch_shape& ls = g_last_shape;
+    ls.consumer = wide ? ATB_CONSUMER_WARPS : drain ? ATB_CONSUMER_DRAIN : ATB_CONSUMER_WARP;
+    ls.release = !drain ? 0u : a.early_release ? ATB_RELEASE_BEFORE_STORE : ATB_RELEASE_AFTER_STORE;
+    ls.stages = stages;
+    ls.store_groups = groups;
+    ls.ctas_per_sm = per_sm;
+    ls.ctas = static_cast<uint32_t>(grid);
+    ls.threads = threads;
+    ls.smem_bytes = static_cast<uint32_t>(smem);
+    ls.boxes = a.n_tiles;
     return ATB_OK;
 }
 
@@ -2011,6 +2033,13 @@ atb_status atb_tile_roundtrip_noalloc(const atb_tensor_map* src, const atb_tenso
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "cudaStreamSynchronize");
     return static_cast<atb_status>(report->code);
+}
+
+atb_status atb_last_launch(atb_launch_shape* out)
+{
+    if (!out) return set_error(ATB_ERR_ARG, "out is NULL");
+    *out = g_last_shape;
+    return ATB_OK;
 }
 
 atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, size_t* bytes)

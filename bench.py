@@ -252,6 +252,7 @@ def run_gpu(args):
     # correctness of the timed configuration before timing it
     with torch.cuda.stream(stream):
         step()
+    launch_shape = atb.last_launch()  # what the library resolved for the timed launches
     stream.synchronize()
     atb.check_device(stream)
     verified = bool(torch.equal(src, dst))
@@ -278,11 +279,14 @@ def run_gpu(args):
     result["config"] = {
         "workload": w.name, "tensor": "16384x16384 fp16 row-major (512 MiB)",
         "box": args.box, "swizzle": w.swizzle, "tiles_per_step": tiles,
-        "stages": args.stages or "library default (3)",
-        "ctas_per_sm": args.ctas_per_sm or "library default (96 KiB of stages per SM)",
-        "store_groups": args.store_groups or "library default (2)", "launch": "programmatic dependent launch",
-        "consumer": ("library default (warp consumer below 32 KiB stages, one-thread drain from 32 KiB)"
-                     if args.consumer == "auto" else args.consumer),
+        "stages": args.stages or "library default",
+        "ctas_per_sm": args.ctas_per_sm or "library default",
+        "store_groups": args.store_groups or "library default",
+        "launch": "programmatic dependent launch",
+        "consumer": ("library default (one-thread drain; for 8-32 KiB stages its own ring: stages for 64 KiB of "
+                     "boxes in load plus 48 KiB of store groups, one CTA per SM, each stage freed before the next "
+                     "store)" if args.consumer == "auto" else args.consumer),
+        "launch_shape": launch_shape,
         "parallelism": f"replicas x{world}",
         "l2": "inputs larger than L2 (512 MiB read + 512 MiB written per step); no flush",
     }
@@ -327,8 +331,14 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
                      (about 96 KiB of stages per SM), two store groups;
       fixed_96KiB    about 96 KiB of stages per SM, split between more stages
                      and fewer CTAs or the reverse;
-      ctas_1, ctas_2 CTAs per SM held at one or two while the ring deepens.
-    A shape that does not fit one CTA's shared memory is reported as infeasible."""
+      ctas_1, ctas_2 CTAs per SM held at one or two while the ring deepens;
+      drain_release_before_store
+                     the one-thread drain freeing each stage before the next
+                     store, one CTA per SM, over stages x store groups (the
+                     library's own drain ring is one of these cells).
+    Every cell but the last row's takes the consumer the library picks for an
+    explicit shape.  A shape that does not fit one CTA's shared memory is
+    reported as infeasible."""
     out = {}
     steps = max(50, min(400, args.steps // 10))
     for w, box in ((datagen.C5A, "64x256"), (datagen.C5B, "128x64_sw128")):
@@ -336,7 +346,7 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
         md = atb.encode_tiled(w.dtype, dst, w.dims, w.strides, w.box, w.swizzle)
         stage_kib = atb.box_bytes(ms) // 1024
 
-        def cell(stages, per_sm, groups=2):
+        def cell(stages, per_sm, groups=2, **kw):
             try:
                 smem = atb.pipeline_smem_bytes(ms, stages)
             except atb.AtbError as e:
@@ -345,7 +355,7 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
                 return f"infeasible: {per_sm} CTAs of {smem} bytes exceed the SM's shared memory"
             g = min(groups, stages)
             sec = time_launches(torch, stream, lambda: atb.tile_roundtrip(
-                ms, md, stream=stream, stages=stages, ctas_per_sm=per_sm, store_groups=g), steps, 5)
+                ms, md, stream=stream, stages=stages, ctas_per_sm=per_sm, store_groups=g, **kw), steps, 5)
             return {"GBps": round(2 * w.storage_bytes * steps / sec / 1e9, 1), "stages": stages, "ctas_per_sm": per_sm,
                     "store_groups": g, "kib_per_sm": stages * stage_kib * per_sm}
 
@@ -360,6 +370,11 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
         for per_sm, key in ((1, "ctas_1"), (2, "ctas_2")):
             for stages in (2, 3, 4, 6, 8, 12):
                 rows[key][f"s{stages}"] = cell(stages, per_sm)
+        # stages - store groups = stages holding boxes being loaded or landed
+        before = ((3, 1), (4, 2), (5, 3), (4, 1), (5, 1)) if stage_kib >= 32 else \
+            ((5, 1), (6, 2), (7, 3), (8, 4), (10, 6), (6, 3), (7, 4), (7, 2), (8, 3))
+        rows["drain_release_before_store"] = {
+            f"s{st}g{g}": cell(st, 1, g, consumer="drain", release="before_store") for st, g in before}
         out[box] = rows
         extra = {}
         for promo in ("128B", "256B"):  # L2 promotion of the source map, default pipeline
@@ -367,7 +382,9 @@ def stage_sweep(torch, atb, datagen, device, stream, src, dst, args):
             sec = time_launches(torch, stream, lambda: atb.tile_roundtrip(mp, md, stream=stream), steps, 5)
             extra[f"l2promotion{promo}"] = round(2 * w.storage_bytes * steps / sec / 1e9, 1)
         for name, kw in (("without_pdl", dict(pdl=False)), ("ring_check", dict(checks=atb.CHECK_RING)),
-                         ("consumer_drain", dict(consumer="drain")), ("consumer_warp", dict(consumer="warp"))):
+                         ("consumer_drain", dict(consumer="drain")), ("consumer_warp", dict(consumer="warp")),
+                         ("release_after_store", dict(consumer="drain", release="after_store")),
+                         ("release_before_store", dict(consumer="drain", release="before_store"))):
             sec = time_launches(torch, stream, lambda: atb.tile_roundtrip(ms, md, stream=stream, **kw), steps, 5)
             extra[name] = round(2 * w.storage_bytes * steps / sec / 1e9, 1)
         out[box]["library_default_variants"] = extra

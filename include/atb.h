@@ -174,7 +174,7 @@ typedef struct {
                                  cp.async.bulk.prefetch.tensor (0 = off) */
     uint32_t checks;          /* ATB_CHECK_* bits: consistency checks inside the kernel (0 = none) */
     uint32_t consumer;        /* tile-grid launches: ATB_CONSUMER_* (0 = the library's choice) */
-    uint32_t reserved[1];
+    uint32_t release;         /* the drain's stage release: ATB_RELEASE_* (0 = the library's choice) */
 } atb_launch;
 
 /*
@@ -201,6 +201,27 @@ typedef struct {
 #define ATB_CONSUMER_AUTO  0u
 #define ATB_CONSUMER_DRAIN 1u
 #define ATB_CONSUMER_WARP  2u
+
+/*
+ * atb_launch.release, for launches the one-thread drain serves: when a stage
+ * whose box is being stored is handed back to the producer.  Other launches
+ * ignore it.
+ *   ATB_RELEASE_AUTO          the library's choice: before the next store on
+ *                             the drain's own ring, after it otherwise
+ *   ATB_RELEASE_AFTER_STORE   after storing box k the drain waits until at
+ *                             most store_groups - 1 groups still read and
+ *                             frees the stage of box k - store_groups + 1
+ *   ATB_RELEASE_BEFORE_STORE  after box k lands the drain pauses for about
+ *                             64 ns, waits until at most store_groups - 1
+ *                             groups still read and frees the stage of box
+ *                             k - store_groups, then stores box k: the load
+ *                             into the freed stage is issued ahead of the
+ *                             store.  Needs store_groups < stages
+ *                             (ATB_ERR_ARG otherwise).
+ */
+#define ATB_RELEASE_AUTO         0u
+#define ATB_RELEASE_AFTER_STORE  1u
+#define ATB_RELEASE_BEFORE_STORE 2u
 
 /*
  * atb_launch.checks bits.
@@ -312,6 +333,37 @@ uint64_t atb_grid_tiles(const atb_tensor_map* map);
  * requested value is still written).
  */
 atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, size_t* bytes);
+
+/*
+ * The launch shape of this host thread's most recent tile load, store or round
+ * trip call (the regular, host-buffer and allocation-free entry points alike):
+ * what the library resolved from atb_launch and its defaults.  All fields are
+ * 0 when that call launched nothing (no boxes, or refused).  Reading it
+ * touches no device.
+ *   consumer      ATB_CONSUMER_DRAIN or ATB_CONSUMER_WARP for tile-grid
+ *                 launches; ATB_CONSUMER_WARPS for launches with several
+ *                 consumer warps (coordinate lists and the fp32 update)
+ *   release       the drain's ATB_RELEASE_AFTER_STORE or
+ *                 ATB_RELEASE_BEFORE_STORE; 0 for the other consumers
+ *   stages, store_groups, ctas_per_sm, ctas (the grid), threads per CTA,
+ *   smem_bytes (dynamic shared memory per CTA), boxes (boxes the launch moves)
+ * ATB_ERR_ARG if out is NULL.
+ */
+#define ATB_CONSUMER_WARPS 3u
+typedef struct {
+    uint32_t consumer;
+    uint32_t release;
+    uint32_t stages;
+    uint32_t store_groups;
+    uint32_t ctas_per_sm;
+    uint32_t ctas;
+    uint32_t threads;
+    uint32_t smem_bytes;
+    uint32_t boxes;
+    uint32_t reserved[3];
+} atb_launch_shape;
+
+atb_status atb_last_launch(atb_launch_shape* out);
 
 /*
  * atb_tile_load -- gather boxes into a packed buffer of shared-memory images.

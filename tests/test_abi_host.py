@@ -47,6 +47,15 @@ def test_struct_layouts(atb):
     assert atb.lib.atb_tensor_map_size() == ctypes.sizeof(atb.TensorMap)
     assert ctypes.sizeof(atb.Launch) == 48
     assert ctypes.sizeof(atb.DeviceReport) == 32
+    assert ctypes.sizeof(atb.LaunchShape) == 48
+
+
+def test_last_launch_is_empty_after_a_refused_call(atb):
+    m = atb.TensorMap()  # never encoded: refused before any launch
+    with pytest.raises(atb.AtbError):
+        atb.tile_roundtrip(m, m)
+    shape = atb.last_launch()
+    assert shape["consumer"] is None and shape["boxes"] == 0 and shape["ctas"] == 0
 
 
 def test_status_strings(atb):
@@ -125,6 +134,9 @@ def test_unknown_launch_options_are_rejected_before_any_device_work(atb):
     with pytest.raises(atb.AtbError) as e:
         atb.tile_roundtrip(m, m, consumer=3)
     assert e.value.code == atb.ATB_ERR_ARG and "consumer" in str(e.value)
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_roundtrip(m, m, release=3)
+    assert e.value.code == atb.ATB_ERR_ARG and "release" in str(e.value)
 
 
 class _FakeDeviceTensor:

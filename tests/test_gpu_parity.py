@@ -145,14 +145,72 @@ def test_c5_full_round_trip_default_launch(atb, w, c5_input, c5_device):
     assert_bytes_equal(host(dst), want, w.name, view=v)
 
 
-@pytest.mark.parametrize("consumer", ["drain", "warp"])
+@pytest.mark.parametrize("consumer", ["drain", "warp", "drain_after_store", "drain_before_store"])
 @pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
 def test_c5_full_round_trip_each_consumer(atb, w, consumer, c5_input, c5_device):
     dst = dev_empty(w.storage_bytes, fill=0)
     ms, md = encode(atb, w, c5_device), encode(atb, w, dst)
-    atb.tile_roundtrip(ms, md, consumer=consumer)
+    kw = dict(consumer=consumer) if "_" not in consumer else \
+        dict(consumer="drain", release=consumer.split("_", 1)[1], stages=5, store_groups=2, ctas_per_sm=1)
+    atb.tile_roundtrip(ms, md, **kw)
     device_ok(atb)
     assert_bytes_equal(host(dst), c5_input, f"{w.name} {consumer}", view=oracle_view(w))
+
+
+def test_library_default_launch_shapes(atb):
+    # What the library resolves for tile-grid round trips of a 32 MiB fp16
+    # tensor (1024 x 16384), per box size, and that each launch moves every byte.
+    dims, strides = (16384, 1024), (2, 32768)
+    src_h = datagen.random_bytes(dims[0] * dims[1] * 2, 77)
+    src = dev_bytes(src_h)
+
+    def run(box, swizzle, **kw):
+        dst = dev_empty(src_h.size, fill=0)
+        ms = atb.encode_tiled("f16", src, dims, strides, box, swizzle)
+        md = atb.encode_tiled("f16", dst, dims, strides, box, swizzle)
+        atb.tile_roundtrip(ms, md, **kw)
+        shape = atb.last_launch()
+        device_ok(atb)
+        assert_bytes_equal(host(dst), src_h, f"box {box} {kw}")
+        return shape
+
+    import torch
+
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    # 16 KiB stages: the drain's own ring, 64 KiB of stages for loads + 48 KiB of store groups
+    s16 = run((64, 128), "128B")
+    assert (s16["consumer"], s16["release"], s16["stages"], s16["store_groups"], s16["ctas_per_sm"]) == \
+        ("drain", "before_store", 7, 3, 1), s16
+    assert s16["ctas"] == sm and s16["boxes"] == 2048
+    # 8 KiB: 8 + 6 stages
+    s8 = run((64, 64), "128B")
+    assert (s8["consumer"], s8["release"], s8["stages"], s8["store_groups"]) == ("drain", "before_store", 14, 6), s8
+    # 32 KiB: the drain on the common default ring, freeing after the store
+    s32 = run((256, 64), "none")
+    assert (s32["consumer"], s32["release"], s32["stages"], s32["store_groups"], s32["ctas_per_sm"]) == \
+        ("drain", "after_store", 3, 2, 1), s32
+    # 4 KiB, or an explicit ring shape below 32 KiB: the warp consumer
+    assert run((64, 32), "128B")["consumer"] == "warp"
+    assert run((64, 128), "128B", stages=3)["consumer"] == "warp"
+    # an explicit order on an explicit ring
+    sb = run((64, 128), "128B", consumer="drain", release="before_store", stages=4, store_groups=3, ctas_per_sm=2)
+    assert (sb["release"], sb["stages"], sb["store_groups"], sb["ctas_per_sm"]) == ("before_store", 4, 3, 2), sb
+    sa = run((64, 128), "128B", consumer="drain", release="after_store")
+    assert (sa["release"], sa["stages"], sa["store_groups"]) == ("after_store", 7, 3), sa
+    # freeing before the next store needs a stage beyond the store groups
+    dst = dev_empty(src_h.size, fill=0)
+    ms = atb.encode_tiled("f16", src, dims, strides, (64, 128), "128B")
+    md = atb.encode_tiled("f16", dst, dims, strides, (64, 128), "128B")
+    with pytest.raises(atb.AtbError) as e:
+        atb.tile_roundtrip(ms, md, consumer="drain", release="before_store", stages=3, store_groups=3)
+    assert e.value.code == atb.ATB_ERR_ARG and "store_groups" in str(e.value)
+    assert atb.last_launch()["boxes"] == 0
+    # coordinate lists run the kernel with several consumer warps
+    coords = dev_bytes(np.array([[0, 0], [64, 128]], dtype=np.int32).reshape(-1).view(np.uint8))
+    packed = dev_empty(2 * 16384, fill=0)
+    atb.tile_load(ms, coords, 2, packed)
+    assert atb.last_launch()["consumer"] == "warps"
+    device_ok(atb)
 
 
 @pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
@@ -242,14 +300,21 @@ def _small_case(name, dtype, dims, box, swizzle, order, seed):
                                     dict(stages=2, ctas=3, schedule="contiguous"), dict(),
                                     dict(prefetch_boxes=3, l2_hints=3, poll_suspend_ns=20000),
                                     dict(checks=1), dict(checks=1, stages=2, ctas=3, store_groups=2),
-                                    dict(consumer="drain"), dict(consumer="warp", stages=2, store_groups=1)],
+                                    dict(consumer="drain"), dict(consumer="warp", stages=2, store_groups=1),
+                                    dict(consumer="drain", release="before_store", stages=2, store_groups=1),
+                                    dict(consumer="drain", release="before_store", stages=4, store_groups=2, ctas=3),
+                                    dict(consumer="drain", release="before_store", stages=5, store_groups=3, ctas=2,
+                                         checks=1, l2_hints=3),
+                                    dict(consumer="drain", release="after_store")],
                          ids=["s1c1", "s3c5g2", "s2c3contig", "default", "prefetch3_hints", "ring_check",
-                              "ring_check_s2c3g2", "drain", "warp_s2g1"])
+                              "ring_check_s2c3g2", "drain", "warp_s2g1", "before_s2g1", "before_s4g2c3",
+                              "before_s5g3c2_check_hints", "drain_after"])
 def test_small_cases_all_ops(atb, case, launch):
     name, dtype, dims, box, swizzle, order = case
     v, src_h, nbytes, coords_h = _small_case(name, dtype, dims, box, swizzle, order, 1000 + len(name))
     if box == (256, 256) and launch.get("stages", 4) > 1:
         launch = dict(launch, stages=1)  # one 128 KiB stage
+        launch.pop("release", None)  # one stage leaves nothing to free before the next store
     src = dev_bytes(src_h)
     coords = dev_bytes(coords_h.view(np.uint8))
     ms = atb.encode_tiled(dtype, src, dims, v.strides, box, swizzle)

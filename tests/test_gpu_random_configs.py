@@ -53,6 +53,10 @@ def draw_case(seed):
     n = int(g.integers(1, 90))
     if seed % 2:  # every other case also runs the stage bookkeeping check (no draw, so cases stay put)
         launch = dict(launch, checks=1)
+    if seed % 3 == 1:  # the one-thread drain where it serves, freeing stages before the next store where it may
+        launch = dict(launch, consumer="drain")
+        if launch.get("stages", 0) > launch.get("store_groups", 0) > 0:
+            launch["release"] = "before_store"
     return dict(dtype=dtype, esize=esize, dims=tuple(dims), strides=tuple(strides), box=tuple(box),
                 swizzle=swizzle, steps=tuple(steps), nbytes=nbytes, launch=launch, n=n, seed=seed)
 
@@ -98,6 +102,10 @@ def draw_large_case(seed):
                   schedule=["strided", "contiguous"][g.integers(2)], checks=int(g.integers(2)))
     if g.random() < 0.3:
         launch = {}
+    if seed % 3 == 2:  # as for the small cases (no draw)
+        launch = dict(launch, consumer="drain")
+        if launch.get("stages", 0) > launch.get("store_groups", 0) > 0:
+            launch["release"] = "before_store"
     return dict(dtype=dtype, esize=esize, dims=tuple(dims), strides=tuple(strides), box=tuple(box),
                 swizzle=swizzle, steps=tuple(steps), nbytes=max(step, 16), launch=launch,
                 n=int(g.integers(1, 2000)), seed=seed)
