@@ -205,7 +205,8 @@ typedef struct {
 /*
  * atb_launch.release, for launches the one-thread drain serves: when a stage
  * whose box is being stored is handed back to the producer.  Other launches
- * ignore it.
+ * ignore it (measured on GB300, freeing before the next store slowed the
+ * several-warp consumer of coordinate lists and the fp32 update by 7-38 %).
  *   ATB_RELEASE_AUTO          the library's choice: before the next store on
  *                             the drain's own ring, after it otherwise
  *   ATB_RELEASE_AFTER_STORE   after storing box k the drain waits until at
