@@ -601,93 +601,41 @@ __device__ void plain_store_grid_box(const PipeArgs& a, const int32_t (&c)[R], u
     }
 }
 
-// Word i (0..3) of a 16-byte value.
-__device__ __forceinline__ uint32_t word_of(const uint4& v, uint32_t i)
-{
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-// Writes bytes [lo, hi) of a 16-byte value to dst + lo .. dst + hi - 1 (dst
-// 16-byte aligned), in the widest aligned stores those bytes allow.
-__device__ __forceinline__ void st_global_part(uint8_t* dst, const uint4& v, uint32_t lo, uint32_t hi)
-{
-    if (lo == 0 && hi == 16) {
-        *reinterpret_cast<uint4*>(dst) = v;
-        return;
-    }
-    while (lo < hi) {
-        const uint32_t n = hi - lo, w = word_of(v, lo >> 2);
-        if ((lo & 7u) == 0 && n >= 8) {
-            *reinterpret_cast<uint64_t*>(dst + lo) = static_cast<uint64_t>(word_of(v, (lo >> 2) + 1)) << 32 | w;
-            lo += 8;
-        } else if ((lo & 3u) == 0 && n >= 4) {
-            *reinterpret_cast<uint32_t*>(dst + lo) = w;
-            lo += 4;
-        } else if ((lo & 1u) == 0 && n >= 2) {
-            *reinterpret_cast<uint16_t*>(dst + lo) = static_cast<uint16_t>(w >> (8 * (lo & 3u)));
-            lo += 2;
-        } else {
-            dst[lo] = static_cast<uint8_t>(w >> (8 * (lo & 3u)));
-            lo += 1;
-        }
-    }
-}
-
 // Where a plain store finds the box in shared memory: the box image (rows of
 // box[0] elements, swizzled like the map), or the one-chunk-wider unswizzled
 // image that the wider map loads from the origin rounded down to the grid.
 enum StoreSource : int { kFromImage = 0, kFromWide = 1 };
 
-// Clipped store of one box into the destination tensor by `nthreads` threads,
-// one aligned 16-byte chunk of the destination row at a time.  A box row
-// starts rb = (x * element size) mod 16 bytes past a 16-byte boundary of the
-// row (rows start on such boundaries: strides are multiples of 16), so it
-// touches box[0] * element size / 16 destination chunks, plus one when rb is
-// not 0.  Destination chunk m holds box bytes 16 m - rb ... 16 m - rb + 15:
-// from the image, the tail of image chunk m - 1 and the head of chunk m (the
-// swizzle moves whole 16-byte chunks), shifted into one value; from the wider
-// image, its chunk m as it is.  Only the bytes inside the box and inside the
-// tensor are written: the chunks at the box's edges and at the row's end take
-// narrower stores, every other chunk one aligned 16-byte store.
-//
-// Threads are laid out as `group` rows of `cols` chunks.  The box is walked
-// plane by plane (dimensions 2..R-1, decomposed once per plane) and, inside a
-// plane, row by row along dimension 1 with additions only.
-template <int R>
-__device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage, int source, uint32_t tid,
-                                uint32_t nthreads)
+// A box whose first row byte is off the 16-byte grid, written into the
+// tensor with aligned stores of U bytes.  U (1, 2 or 4) is the largest power
+// of two up to 4 that divides both that row byte and the tensor row's byte
+// length, so every U-byte unit lies wholly inside or wholly outside the
+// tensor and no store reaches a byte outside the box.  Each consumer warp
+// takes whole box rows and its lanes the row's units: one store instruction
+// writes 32 U contiguous bytes of a row.  A unit's place in the stage follows
+// from its byte offset in the row: in the box image (swizzled like the map)
+// or in the wider unswizzled image, where the box's row starts rb bytes in.
+constexpr uint32_t kRowsInFlight = 4;
+
+template <int R, uint32_t U>
+__device__ void store_units(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage, int source, uint32_t tid,
+                            uint32_t nthreads)
 {
     const uint32_t es = a.esize;
     const uint32_t row_bytes = a.box[0] * es;  // the innermost step is always 1
-    const uint32_t cpr = row_bytes / 16;        // image chunks per row
-    const uint32_t rb = row_phase<R>(a, c);
-    const uint32_t cg = cpr + (rb ? 1u : 0u);   // destination chunks a box row touches
+    const uint32_t upr = row_bytes / U;        // units per box row
     const uint32_t rows1 = R > 1 ? a.visits[1] : 1;
-    const uint32_t planes = a.box_bytes / (row_bytes * rows1);
+    uint32_t planes = 1;
+#pragma unroll
+    for (int d = 2; d < R; ++d) planes *= a.visits[d];
     const uint32_t pitch = source == kFromWide ? a.wide_pitch : row_bytes;
+    const uint32_t src0 = source == kFromWide ? row_phase<R>(a, c) : 0u;
     const uint32_t line_mask = source == kFromWide ? 0u : (1u << a.swizzle_bits) - 1u;
+    const int64_t gx0 = static_cast<int64_t>(c[0]) * es;
     const int64_t row_end = static_cast<int64_t>(a.dst_dims[0]) * es;
-    const int64_t gx0 = static_cast<int64_t>(c[0]) * es;  // row byte of the box's first element
-    const int64_t base_b = gx0 - rb;                       // row byte of destination chunk 0
-    // box bytes inside the row, relative to destination chunk 0
-    const int64_t in_lo = (gx0 > 0 ? gx0 : 0) - base_b;
-    const int64_t in_hi = (gx0 + row_bytes < row_end ? gx0 + row_bytes : row_end) - base_b;
-    if (in_lo >= in_hi) return;
-    const uint32_t cols = cg < nthreads ? cg : nthreads;
-    const uint32_t group = nthreads / cols;
-    const uint32_t first_row = tid / cols;
-    if (first_row >= group) return;  // threads beyond group * cols have no chunk
-    const uint32_t m0 = tid - first_row * cols;
     const int64_t dims1 = R > 1 ? static_cast<int64_t>(a.dst_dims[1]) : 1;
-    const int64_t gstep1 = R > 1 ? static_cast<int64_t>(group) * a.step[1] : 0;
     const uint64_t stride1 = R > 1 ? a.dst_strides[1] : 0;
-
-    // the smem offset of chunk j of the row that starts at r_off
-    auto chunk_at = [&](uint32_t r_off, uint32_t j) {
-        const uint32_t o = r_off + 16 * j;
-        return stage + (o ^ (((o >> 7) & line_mask) << 4));
-    };
-    const bool pair = source == kFromImage && rb != 0;  // two image chunks make one destination chunk
+    const uint32_t warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
 
     for (uint32_t plane = 0; plane < planes; ++plane) {
         uint32_t rest = plane;
@@ -695,79 +643,86 @@ __device__ void plain_store_box(const PipeArgs& a, const int32_t (&c)[R], uint32
         uint64_t plane_addr = 0;
 #pragma unroll
         for (int d = 2; d < R; ++d) {
-            const uint32_t k = rest % a.visits[d];
-            rest /= a.visits[d];
+            const uint32_t k = planes == 1 ? 0u : rest % a.visits[d];
+            if (planes != 1) rest /= a.visits[d];
             const int64_t g = static_cast<int64_t>(c[d]) + static_cast<int64_t>(k) * a.step[d];
             if (g < 0 || g >= static_cast<int64_t>(a.dst_dims[d])) inside = false;
             else plane_addr += static_cast<uint64_t>(g) * a.dst_strides[d];
         }
         if (!inside) continue;
-        // destination chunk 0 of the box's rows in this plane (it may lie
-        // before the row: only bytes from in_lo on are ever written)
-        uint8_t* chunk0 = a.dst_base + plane_addr + static_cast<uint64_t>(base_b);
-        const uint32_t plane_off = plane * rows1 * pitch;
-        if (cg <= nthreads) {
-            // One destination column per thread: its byte range, its image
-            // chunks and its whole-or-part decision are fixed for the box.
-            // Four rows at a time: their shared loads are issued before any
-            // shift or store.
-            const uint32_t m = m0;
-            const int64_t lo64 = in_lo - 16 * static_cast<int64_t>(m), hi64 = in_hi - 16 * static_cast<int64_t>(m);
-            if (hi64 <= 0 || lo64 >= 16) return;
-            const uint32_t lo = lo64 > 0 ? static_cast<uint32_t>(lo64) : 0u;
-            const uint32_t hi = hi64 < 16 ? static_cast<uint32_t>(hi64) : 16u;
-            const bool whole = lo == 0 && hi == 16;
-            const bool has_a = pair && m >= 1, has_b = !pair || m < cpr;
-            uint8_t* col = chunk0 + 16 * m;
-            constexpr int U = 4;
-            for (uint32_t k1 = first_row; k1 < rows1; k1 += U * group) {
-                uint4 A[U], B[U];
-                bool row_in[U];
-                uint8_t* dst[U];
+        uint8_t* const plane_dst = a.dst_base + plane_addr;
+        const uint32_t plane_off = plane * rows1 * pitch + src0;
+        // kRowsInFlight rows of the warp at a time: their shared loads are all
+        // issued before the first global store (one load latency per batch).
+        if (upr <= 32) {  // one unit per lane: its place in the row is fixed for the box
+            const uint32_t k = lane;
+            const int64_t x = gx0 + static_cast<int64_t>(k * U);
+            const bool x_in = k < upr && x >= 0 && x < row_end;
+            const uint32_t o_k = plane_off + k * U;
+            for (uint32_t k1 = warp; k1 < rows1; k1 += kRowsInFlight * nwarps) {
+                uint32_t v[kRowsInFlight];
+                uint8_t* dst[kRowsInFlight];
+                bool in[kRowsInFlight];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const uint32_t kk = k1 + u * group;
+                for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+                    const uint32_t kk = k1 + u * nwarps;
                     const int64_t g1 = R > 1 ? static_cast<int64_t>(c[1]) + static_cast<int64_t>(kk) * a.step[1] : 0;
-                    row_in[u] = kk < rows1 && g1 >= 0 && g1 < dims1;
-                    dst[u] = col + static_cast<uint64_t>(row_in[u] ? g1 : 0) * stride1;
-                    const uint32_t r_off = plane_off + kk * pitch;
-                    A[u] = make_uint4(0, 0, 0, 0);
-                    B[u] = make_uint4(0, 0, 0, 0);
-                    if (row_in[u] && has_a) A[u] = ptx::ld_shared_v4_u32(chunk_at(r_off, m - 1));
-                    if (row_in[u] && has_b) B[u] = ptx::ld_shared_v4_u32(chunk_at(r_off, m));
+                    in[u] = x_in && kk < rows1 && g1 >= 0 && g1 < dims1;
+                    dst[u] = plane_dst + static_cast<uint64_t>(in[u] ? g1 : 0) * stride1 + x;
+                    const uint32_t o = o_k + kk * pitch;
+                    const uint32_t p = stage + (o ^ (((o >> 7) & line_mask) << 4));
+                    v[u] = 0;
+                    if (in[u]) v[u] = U == 4 ? ptx::ld_shared_u32(p) : U == 2 ? ptx::ld_shared_u16(p) : ptx::ld_shared_u8(p);
                 }
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (!row_in[u]) continue;
-                    const uint4 v = pair ? bytes_from_pair(A[u], B[u], 16 - rb) : B[u];
-                    if (whole) *reinterpret_cast<uint4*>(dst[u]) = v;
-                    else st_global_part(dst[u], v, lo, hi);
+                for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+                    if (!in[u]) continue;
+                    if (U == 4) *reinterpret_cast<uint32_t*>(dst[u]) = v[u];
+                    else if (U == 2) *reinterpret_cast<uint16_t*>(dst[u]) = static_cast<uint16_t>(v[u]);
+                    else *dst[u] = static_cast<uint8_t>(v[u]);
                 }
             }
             continue;
         }
-        int64_t g1 = R > 1 ? static_cast<int64_t>(c[1]) + static_cast<int64_t>(first_row) * a.step[1] : 0;
-        uint32_t r_off = plane_off + first_row * pitch;
-        const uint32_t r_step = group * pitch;
-        for (uint32_t k1 = first_row; k1 < rows1; k1 += group, g1 += gstep1, r_off += r_step) {
-            if (g1 < 0 || g1 >= dims1) continue;
-            uint8_t* row = chunk0 + static_cast<uint64_t>(g1) * stride1;
-            for (uint32_t m = m0; m < cg; m += cols) {
-                const int64_t lo = in_lo - 16 * static_cast<int64_t>(m);
-                const int64_t hi = in_hi - 16 * static_cast<int64_t>(m);
-                if (hi <= 0 || lo >= 16) continue;
-                uint4 v;
-                if (!pair) {
-                    v = ptx::ld_shared_v4_u32(chunk_at(r_off, m));
-                } else {
-                    const uint4 A = m >= 1 ? ptx::ld_shared_v4_u32(chunk_at(r_off, m - 1)) : make_uint4(0, 0, 0, 0);
-                    const uint4 B = m < cpr ? ptx::ld_shared_v4_u32(chunk_at(r_off, m)) : make_uint4(0, 0, 0, 0);
-                    v = bytes_from_pair(A, B, 16 - rb);
+        for (uint32_t k1 = warp; k1 < rows1; k1 += kRowsInFlight * nwarps) {
+            for (uint32_t k = lane; k < upr; k += 32) {
+                const int64_t x = gx0 + static_cast<int64_t>(k * U);
+                const bool x_in = x >= 0 && x < row_end;
+                uint32_t v[kRowsInFlight];
+                uint8_t* dst[kRowsInFlight];
+                bool in[kRowsInFlight];
+#pragma unroll
+                for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+                    const uint32_t kk = k1 + u * nwarps;
+                    const int64_t g1 = R > 1 ? static_cast<int64_t>(c[1]) + static_cast<int64_t>(kk) * a.step[1] : 0;
+                    in[u] = x_in && kk < rows1 && g1 >= 0 && g1 < dims1;
+                    dst[u] = plane_dst + static_cast<uint64_t>(in[u] ? g1 : 0) * stride1 + x;
+                    const uint32_t o = plane_off + kk * pitch + k * U;
+                    const uint32_t p = stage + (o ^ (((o >> 7) & line_mask) << 4));
+                    v[u] = 0;
+                    if (in[u]) v[u] = U == 4 ? ptx::ld_shared_u32(p) : U == 2 ? ptx::ld_shared_u16(p) : ptx::ld_shared_u8(p);
                 }
-                st_global_part(row + 16 * m, v, lo > 0 ? static_cast<uint32_t>(lo) : 0u,
-                               hi < 16 ? static_cast<uint32_t>(hi) : 16u);
+#pragma unroll
+                for (uint32_t u = 0; u < kRowsInFlight; ++u) {
+                    if (!in[u]) continue;
+                    if (U == 4) *reinterpret_cast<uint32_t*>(dst[u]) = v[u];
+                    else if (U == 2) *reinterpret_cast<uint16_t*>(dst[u]) = static_cast<uint16_t>(v[u]);
+                    else *dst[u] = static_cast<uint8_t>(v[u]);
+                }
             }
         }
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void store_off_grid_box(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage,
+                                                   int source, uint32_t tid, uint32_t nthreads)
+{
+    const uint32_t bits = static_cast<uint32_t>(c[0]) * a.esize | a.dst_dims[0] * a.esize | 4u;
+    switch (bits & (~bits + 1u)) {  // the lowest set bit: 1, 2 or 4
+    case 1: store_units<R, 1>(a, c, stage, source, tid, nthreads); break;
+    case 2: store_units<R, 2>(a, c, stage, source, tid, nthreads); break;
+    default: store_units<R, 4>(a, c, stage, source, tid, nthreads); break;
     }
 }
 
@@ -1418,10 +1373,10 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
         if (kind == kStorePlain) {
             if (MODE == kLoad)
                 pack_from_wide<R>(a, c, r.stage(s), a.packed + static_cast<size_t>(cur.t) * a.box_bytes, ct, CT);
-            else if (!LISTED)  // tile-grid origins sit on the 16-byte grid
+            else if (LISTED && row_phase<R>(a, c))  // off the 16-byte grid: aligned stores of up to 4 bytes
+                store_off_grid_box<R>(a, c, r.stage(s), wide ? kFromWide : kFromImage, ct, CT);
+            else  // on the 16-byte grid: 16-byte chunks
                 plain_store_grid_box<R>(a, c, r.stage(s), ct, CT);
-            else
-                plain_store_box<R>(a, c, r.stage(s), wide ? kFromWide : kFromImage, ct, CT);
             ptx::named_barrier_sync(1, CT);  // every reader is done with the stage
         }
         if (ct == 0) {
