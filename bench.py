@@ -495,7 +495,24 @@ def workload_lines(torch, atb, datagen, device, stream, args):
         warm, cold = timed(lambda: atb.tile_roundtrip(ms, mf, coords, n, stream=stream), 500, 30)
         out[w.name + tag + "_roundtrip"] = line(2 * inb, n, warm, cold)
         del packed
-    out["fixed_cost_fits"] = fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src, ms)
+    fits = fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src, ms, mf)
+    out["fixed_cost_fits"] = fits
+    # every short line's fraction of the measured copy peak after an L2 flush, whole and net of the fixed
+    # cost T0 fitted for its kind of launch
+    peak, _ = hbm_peak()
+    for name, fit_key in ((datagen.C2.name, "c2_round_trip"), (datagen.C2.name + "_library_default_grid",
+                                                               "c2_round_trip"),
+                          (datagen.C3.name, "c3_gather"), (w.name + "_load", "c4_gather"),
+                          (w.name + "_store", "c4_store"), (w.name + "_roundtrip", "c4_roundtrip"),
+                          (w.name + "_grid16B_origins_load", "c4_gather"),
+                          (w.name + "_grid16B_origins_store", "c4_store"),
+                          (w.name + "_grid16B_origins_roundtrip", "c4_roundtrip")):
+        ln, t0 = out[name], fits[fit_key]["fixed_us"] * 1e-6
+        cold = ln["l2_flushed"]["us"] * 1e-6
+        ln["l2_flushed"]["frac_of_peak"] = round(ln["bytes_per_launch"] / cold / 1e9 / peak, 3)
+        ln["l2_flushed"]["net_of_fixed"] = {"fixed_us": fits[fit_key]["fixed_us"], "fit": fit_key,
+                                            "frac_of_peak": round(ln["bytes_per_launch"] / max(cold - t0, 1e-9)
+                                                                  / 1e9 / peak, 3)}
     del src, fresh
 
     # the fp32 update between load and store: 16384 x 8192 fp32 (512 MiB), box 32x128, 128B swizzle
@@ -532,7 +549,7 @@ def workload_lines(torch, atb, datagen, device, stream, args):
     return out
 
 
-def fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src4, ms4):
+def fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src4, ms4, mf4):
     """Each short launch as T(n) = T0 + n * t: the same launch over n boxes for
     several n, timed after an L2 flush, and a least-squares line through the
     points.  T0 is what a launch costs before and around its boxes (launch,
@@ -565,9 +582,25 @@ def fixed_cost_fits(torch, atb, datagen, device, stream, timed, dev_bytes, src4,
     bb = atb.box_bytes(ms4)
     packed = torch.empty(len(coords_h) * bb, dtype=torch.uint8, device=device)
     inb_per_box = box_inbound_bytes(w.dims, w.box, w.esize, coords_h) / len(coords_h)
-    out = {"c4_gather": fit("workload 4 gather, first n of its 4096 listed boxes", (512, 1024, 2048, 3072, 4096),
-                            inb_per_box + bb,
-                            lambda n: (lambda: atb.tile_load(ms4, coords, n, packed, stream=stream)))}
+    ns4 = (512, 1024, 2048, 3072, 4096)
+    out = {"c4_gather": fit("workload 4 gather, first n of its 4096 listed boxes", ns4, inb_per_box + bb,
+                            lambda n: (lambda: atb.tile_load(ms4, coords, n, packed, stream=stream))),
+           "c4_store": fit("workload 4 store, first n of its 4096 listed boxes", ns4, inb_per_box + bb,
+                           lambda n: (lambda: atb.tile_store(mf4, coords, n, packed, stream=stream))),
+           "c4_roundtrip": fit("workload 4 round trip, first n of its 4096 listed boxes", ns4, 2 * inb_per_box,
+                               lambda n: (lambda: atb.tile_roundtrip(ms4, mf4, coords, n, stream=stream)))}
+    # workload 3 over its first box rows (47 boxes each, the last column ragged)
+    w = datagen.C3
+    src3 = dev_bytes(datagen.storage(w))
+    maps3 = {}
+    for box_rows in (10, 20, 40, 60, 78):
+        m3 = atb.encode_tiled(w.dtype, src3, (w.dims[0], box_rows * w.box[1]), w.strides, w.box, w.swizzle)
+        maps3[atb.grid_tiles(m3)] = m3
+    n3max = max(maps3)
+    packed3 = torch.empty(n3max * atb.box_bytes(m3), dtype=torch.uint8, device=device)
+    per_box3 = (w.dims[0] * 2 * w.box[1] * 78) / n3max + atb.box_bytes(m3)  # in-bound bytes + image, per box
+    out["c3_gather"] = fit("workload 3 gather over its first box rows", sorted(maps3), per_box3,
+                           lambda n: (lambda: atb.tile_load(maps3[n], None, 0, packed3, stream=stream)))
     # workload 2 over its first rows: the same 64 x 256 boxes, n = 7 column tiles x row strips
     w = datagen.C2
     src2 = dev_bytes(datagen.storage(w))
