@@ -503,11 +503,9 @@ __device__ void thread_load_box(const PipeArgs& a, const int32_t (&c)[R], uint32
     }
 }
 
-// Clipped store of one tile-grid box image from shared memory by `nthreads`
-// threads, 16 bytes at a time (the tile-grid kernel's own copy: it only sees
-// origins on the 16-byte grid, and on GB300 its round trips moved more bytes
-// per second with this loop than with the general one below, which it never
-// runs either way).  The swizzle moves whole 16-byte chunks (the chunk
+// Clipped store of one box image whose x origin is on the 16-byte grid (every
+// tile-grid box, and listed boxes on that grid) from shared memory by
+// `nthreads` threads, 16 bytes at a time.  The swizzle moves whole 16-byte chunks (the chunk
 // number, bits 4..6 of the image offset, is XORed with the low swizzle bits of
 // the 128-byte line number, bits 7..9), and a box row starts on a 16-byte
 // boundary in both spaces (the origin's x is 16-byte aligned, strides are
@@ -517,8 +515,9 @@ __device__ void thread_load_box(const PipeArgs& a, const int32_t (&c)[R], uint32
 // Threads are laid out as `group` rows of `cpr` chunks (or, for rows wider
 // than the thread count, one row at a time).  The box is walked plane by plane
 // (dimensions 2..R-1, decomposed once per plane) and, inside a plane, row by
-// row along dimension 1 with additions only: a single warp runs this loop
-// alone, so short dependency chains matter more than instruction counts.
+// row along dimension 1 with additions only: in the warp consumer a single
+// warp runs this loop alone, so short dependency chains matter more than
+// instruction counts.
 template <int R>
 __device__ void plain_store_grid_box(const PipeArgs& a, const int32_t (&c)[R], uint32_t stage, uint32_t tid,
                                 uint32_t nthreads)
