@@ -1319,7 +1319,11 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
             failed = true;
             break;
         }
-        if (ct == 0) ring_check_filled(a, r, s, k, cur.t);
+        if (ct == 0) {
+            ring_check_filled(a, r, s, k, cur.t);
+            if (a.early_release)  // free the stage of every box stored at least store_groups boxes back
+                pending.retire(a, r, k, a.store_lag + 1);
+        }
         const int lk = !LISTED          ? kLoadEngine
                        : MODE == kStore ? (origin_error<R>(a, c) ? kLoadRefused : kLoadEngine)
                                         : load_kind<R>(a, c);
@@ -1393,7 +1397,7 @@ __global__ void __launch_bounds__(32 + (ADD ? kUpdateConsumerThreads : kConsumer
                 ring_note_freed(a, r, s, k);
                 ptx::mbar_arrive(r.empty(s));  // written by the threads, or nothing to write
             }
-            pending.retire(a, r, k, a.store_lag);
+            if (!a.early_release) pending.retire(a, r, k, a.store_lag);
         }
     }
 
@@ -1496,6 +1500,18 @@ constexpr uint32_t kDrainStageBytes = 32u * 1024u;
 constexpr uint32_t kDrainMinStageBytes = 8u * 1024u;
 constexpr uint32_t kDrainLoadSideBytes = 64u * 1024u;
 constexpr uint32_t kDrainStoreSideBytes = 48u * 1024u;
+
+// The several-warp kernel's own ring (coordinate lists and the fp32 update) for
+// stages of 16 to 32 KiB, measured the same way: two CTAs per SM (its consumer
+// warps' per-box work needs another CTA's boxes to hide behind), each with
+// 32 KiB of stages for boxes being loaded or landed (64 KiB per SM again) and
+// 48 KiB of store groups, stages freed before the next store.  16 KiB boxes:
+// fp32 update 6,343 -> 6,564 GB/s and listed gather 6,344 -> 6,644 against the
+// common ring (same GPU); 48 KiB per CTA on the load side fell to 5,870-6,160.
+constexpr uint32_t kWideDeepMinStageBytes = 16u * 1024u;
+constexpr uint32_t kWideLoadSideBytes = 32u * 1024u;
+constexpr uint32_t kWideStoreSideBytes = 48u * 1024u;
+constexpr uint32_t kWideDeepCtasPerSm = 2;
 
 uint32_t default_stages(const atb_tensor_map* m, const DeviceInfo& dev, bool wide_loads)
 {
@@ -1644,10 +1660,17 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     const bool deep_fits = !shape_given && stage_b >= kDrainMinStageBytes && stage_b < kDrainStageBytes;
     const bool drain = drain_fits && (consumer == ATB_CONSUMER_DRAIN ||
                                       (consumer == ATB_CONSUMER_AUTO && (stage_b >= kDrainStageBytes || deep_fits)));
-    const bool deep = drain && deep_fits;
-    const uint32_t deep_groups = deep ? kDrainStoreSideBytes / stage_b : 0u;
+    const bool deep = drain && deep_fits;  // the drain's own ring
+    // the several-warp kernel's own ring (coordinate lists and the fp32 update, 16 to 32 KiB stages)
+    // (sized on the box image: off-grid listed boxes load a wider image into the same number of stages)
+    const uint32_t image_b = stage_bytes_for(shape);
+    const bool wide_deep = wide && !shape_given && image_b >= kWideDeepMinStageBytes && image_b < kDrainStageBytes;
+    const uint32_t deep_groups = deep ? kDrainStoreSideBytes / stage_b
+                                 : wide_deep ? kWideStoreSideBytes / image_b
+                                             : 0u;
     const uint32_t stages = cfg && cfg->stages ? cfg->stages
                             : deep             ? kDrainLoadSideBytes / stage_b + deep_groups
+                            : wide_deep        ? kWideLoadSideBytes / image_b + deep_groups
                                                : default_stages(shape, dev, wide_loads);
     if (stages < 1 || stages > kMaxStages)
         return set_error(ATB_ERR_ARG, "stages = %u is outside 1..%u", stages, kMaxStages);
@@ -1656,15 +1679,18 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         return set_error(ATB_ERR_SMEM_BUDGET,
                          "%u stages of %u bytes need %zu bytes of shared memory; a block may have at most %d",
                          stages, stage_b, smem, dev.smem_optin);
-    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups : deep ? deep_groups : kDefaultStoreGroups;
+    uint32_t groups = cfg && cfg->store_groups ? cfg->store_groups
+                      : deep || wide_deep        ? deep_groups
+                                                 : kDefaultStoreGroups;
     if (groups > stages) groups = stages;
     if (groups > 8) groups = 8;
     const uint32_t release = cfg ? cfg->release : ATB_RELEASE_AUTO;
-    if (drain && release == ATB_RELEASE_BEFORE_STORE && groups >= stages)
+    const bool releases = drain || wide;  // the consumers that honour atb_launch.release
+    if (releases && release == ATB_RELEASE_BEFORE_STORE && groups >= stages)
         return set_error(ATB_ERR_ARG, "releasing before the next store needs store_groups (%u) < stages (%u)", groups,
                          stages);
-    const bool early =
-        drain && groups < stages && (release == ATB_RELEASE_BEFORE_STORE || (release == ATB_RELEASE_AUTO && deep));
+    const bool early = releases && groups < stages &&
+                       (release == ATB_RELEASE_BEFORE_STORE || (release == ATB_RELEASE_AUTO && (deep || wide_deep)));
     if (n_tiles == 0) return ATB_OK;
 
     DeviceStatus* status = caller_status;
@@ -1688,7 +1714,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     st = kernel_fit(fn, dev, threads, smem, &fit);
     if (st != ATB_OK) return st;
 
-    uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm : deep ? 1u : 0u;
+    uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm : deep ? 1u : wide_deep ? kWideDeepCtasPerSm : 0u;
     if (!per_sm) {
         // sized on the box image: a wider stage for off-grid loads does not cut the CTA count
         uint64_t want = kStageBytesPerSm / (static_cast<uint64_t>(stages) * stage_bytes_for(shape));
@@ -1775,7 +1801,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     atb_launch_shape& ls = g_last_shape;
     ls.consumer = wide ? ATB_CONSUMER_WARPS : drain ? ATB_CONSUMER_DRAIN : ATB_CONSUMER_WARP;
-    ls.release = !drain ? 0u : a.early_release ? ATB_RELEASE_BEFORE_STORE : ATB_RELEASE_AFTER_STORE;
+    ls.release = !(drain || wide) ? 0u : a.early_release ? ATB_RELEASE_BEFORE_STORE : ATB_RELEASE_AFTER_STORE;
     ls.stages = stages;
     ls.store_groups = groups;
     ls.ctas_per_sm = per_sm;

@@ -203,22 +203,26 @@ typedef struct {
 #define ATB_CONSUMER_WARP  2u
 
 /*
- * atb_launch.release, for launches the one-thread drain serves: when a stage
- * whose box is being stored is handed back to the producer.  Other launches
- * ignore it (measured on GB300, freeing before the next store slowed the
- * several-warp consumer of coordinate lists and the fp32 update by 7-38 %).
+ * atb_launch.release, for launches the one-thread drain or the several-warp
+ * consumer (coordinate lists, the fp32 update) serves: when a stage whose box
+ * is being stored is handed back to the producer.  The warp consumer ignores
+ * it.
  *   ATB_RELEASE_AUTO          the library's choice: before the next store on
- *                             the drain's own ring, after it otherwise
- *   ATB_RELEASE_AFTER_STORE   after storing box k the drain waits until at
+ *                             the drain's own ring and on the several-warp
+ *                             consumer's own ring (16-32 KiB stages, no shape
+ *                             given: two CTAs per SM, 32 KiB of stages for
+ *                             boxes being loaded or landed and 48 KiB of
+ *                             store groups each), after it otherwise
+ *   ATB_RELEASE_AFTER_STORE   after storing box k the consumer waits until at
  *                             most store_groups - 1 groups still read and
  *                             frees the stage of box k - store_groups + 1
- *   ATB_RELEASE_BEFORE_STORE  after box k lands the drain pauses for about
- *                             64 ns, waits until at most store_groups - 1
- *                             groups still read and frees the stage of box
- *                             k - store_groups, then stores box k: the load
- *                             into the freed stage is issued ahead of the
- *                             store.  Needs store_groups < stages
- *                             (ATB_ERR_ARG otherwise).
+ *   ATB_RELEASE_BEFORE_STORE  after box k lands the consumer waits until at
+ *                             most store_groups - 1 groups still read and
+ *                             frees the stage of box k - store_groups, then
+ *                             stores box k: the load into the freed stage is
+ *                             issued ahead of the store (the drain first
+ *                             pauses for about 64 ns).  Needs store_groups <
+ *                             stages (ATB_ERR_ARG otherwise).
  */
 #define ATB_RELEASE_AUTO         0u
 #define ATB_RELEASE_AFTER_STORE  1u

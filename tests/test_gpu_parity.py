@@ -210,9 +210,10 @@ def test_library_default_launch_shapes(atb):
     packed = dev_empty(2 * 16384, fill=0)
     atb.tile_load(ms, coords, 2, packed)
     sl = atb.last_launch()
-    assert (sl["consumer"], sl["release"], sl["boxes"]) == ("warps", None, 2), sl
+    assert (sl["consumer"], sl["release"], sl["stages"], sl["store_groups"], sl["ctas_per_sm"], sl["boxes"]) == \
+        ("warps", "before_store", 5, 3, 2, 2), sl
     device_ok(atb)
-    # the fp32 update over the tile grid keeps the common ring (16 KiB boxes of fp32)
+    # the fp32 update over the tile grid takes the several-warp kernel's own ring (16 KiB boxes of fp32)
     fv = oracle.View(4, (8192, 512), (4, 32768), (32, 128), "128B")
     f_h = datagen.finite_f32_bytes(8192 * 512, 78)
     fsrc, fdst = dev_bytes(f_h), dev_empty(f_h.size, fill=0)
@@ -221,11 +222,11 @@ def test_library_default_launch_shapes(atb):
     atb.tile_roundtrip_add_f32(mfs, mfd, 1.0)
     sf = atb.last_launch()
     assert (sf["consumer"], sf["release"], sf["stages"], sf["store_groups"], sf["ctas_per_sm"]) == \
-        ("warps", None, 3, 2, 2), sf
+        ("warps", "before_store", 5, 3, 2), sf
     device_ok(atb)
     want = np.zeros_like(f_h)
     oracle.roundtrip_add_f32(fv, f_h, fv, want, oracle.grid_coords(fv), 1.0)
-    assert_bytes_equal(host(fdst), want, "fp32 update on the common ring", view=fv)
+    assert_bytes_equal(host(fdst), want, "fp32 update on the several-warp ring", view=fv)
 
 
 @pytest.mark.parametrize("w", [datagen.C5A, datagen.C5B], ids=["box64x256", "box128x64_sw128"])
