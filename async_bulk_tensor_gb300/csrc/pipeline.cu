@@ -1496,10 +1496,17 @@ constexpr uint32_t kDrainStageBytes = 32u * 1024u;
 // freed before the next store is issued so that the load into it goes out
 // first.  Every ring with four stages on the load side and three to six
 // store groups sustained 6,786-6,796 GB/s; three or five load-side stages
-// fell to 6,190-6,240.
-constexpr uint32_t kDrainMinStageBytes = 8u * 1024u;
+// fell to 6,190-6,240.  Stages of 4 to 8 KiB would need more stages than a
+// ring holds; they run two CTAs per SM, each with 32 KiB of stages on the load
+// side (64 KiB per SM again) and 16 KiB of store groups (4 KiB boxes: 6,297-
+// 6,341 GB/s against 6,199-6,291 for the warp consumer, the step-2 gather
+// 5,552 -> 6,355; 24 KiB of store groups per CTA measured 5,984-6,162).
+constexpr uint32_t kDrainMinStageBytes = 4u * 1024u;
 constexpr uint32_t kDrainLoadSideBytes = 64u * 1024u;
 constexpr uint32_t kDrainStoreSideBytes = 48u * 1024u;
+constexpr uint32_t kDrainSmallStageBytes = 8u * 1024u;  // below: two CTAs per SM
+constexpr uint32_t kDrainSmallLoadSideBytes = 32u * 1024u;
+constexpr uint32_t kDrainSmallStoreSideBytes = 16u * 1024u;
 
 // The several-warp kernel's own ring (coordinate lists and the fp32 update) for
 // stages of 16 to 32 KiB, measured the same way: two CTAs per SM (its consumer
@@ -1639,8 +1646,9 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     // Tile grid: where every box leaves through one engine copy (no box misses
     // the destination or crosses a ragged row end) either consumer serves.
     // The library takes the one-thread drain for stages of 32 KiB and more,
-    // and for stages of 8 to 32 KiB when the caller leaves the ring's shape to
-    // it (the drain then runs its own deeper ring, one CTA per SM); the warp
+    // and for stages of 4 to 32 KiB when the caller leaves the ring's shape to
+    // it (the drain then runs its own deeper ring, one CTA per SM, two below
+    // 8 KiB); the warp
     // consumer otherwise (measured on GB300: each was the faster there).  The
     // warp consumer, which can also write plain clipped stores, serves the
     // rest.  The drain's producer neither prefetches nor suspends its polls:
@@ -1665,10 +1673,13 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     // (sized on the box image: off-grid listed boxes load a wider image into the same number of stages)
     const uint32_t image_b = stage_bytes_for(shape);
     const bool wide_deep = wide && !shape_given && image_b >= kWideDeepMinStageBytes && image_b < kDrainStageBytes;
-    const uint32_t deep_groups = deep ? kDrainStoreSideBytes / stage_b
+    const bool deep_small = deep && stage_b < kDrainSmallStageBytes;
+    const uint32_t deep_groups = deep_small ? kDrainSmallStoreSideBytes / stage_b
+                                 : deep     ? kDrainStoreSideBytes / stage_b
                                  : wide_deep ? kWideStoreSideBytes / image_b
                                              : 0u;
     const uint32_t stages = cfg && cfg->stages ? cfg->stages
+                            : deep_small       ? kDrainSmallLoadSideBytes / stage_b + deep_groups
                             : deep             ? kDrainLoadSideBytes / stage_b + deep_groups
                             : wide_deep        ? kWideLoadSideBytes / image_b + deep_groups
                                                : default_stages(shape, dev, wide_loads);
@@ -1714,7 +1725,11 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     st = kernel_fit(fn, dev, threads, smem, &fit);
     if (st != ATB_OK) return st;
 
-    uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm : deep ? 1u : wide_deep ? kWideDeepCtasPerSm : 0u;
+    uint32_t per_sm = cfg && cfg->ctas_per_sm ? cfg->ctas_per_sm
+                      : deep_small               ? 2u
+                      : deep                     ? 1u
+                      : wide_deep                ? kWideDeepCtasPerSm
+                                                 : 0u;
     if (!per_sm) {
         // sized on the box image: a wider stage for off-grid loads does not cut the CTA count
         uint64_t want = kStageBytesPerSm / (static_cast<uint64_t>(stages) * stage_bytes_for(shape));

@@ -283,9 +283,9 @@ def run_gpu(args):
         "ctas_per_sm": args.ctas_per_sm or "library default",
         "store_groups": args.store_groups or "library default",
         "launch": "programmatic dependent launch",
-        "consumer": ("library default (one-thread drain; for 8-32 KiB stages its own ring: stages for 64 KiB of "
-                     "boxes in load plus 48 KiB of store groups, one CTA per SM, each stage freed before the next "
-                     "store)" if args.consumer == "auto" else args.consumer),
+        "consumer": ("library default (one-thread drain; for 4-32 KiB stages its own ring: 64 KiB of stages per SM "
+                     "for boxes in load plus store groups, each stage freed before the next store)"
+                     if args.consumer == "auto" else args.consumer),
         "launch_shape": launch_shape,
         "parallelism": f"replicas x{world}",
         "l2": "inputs larger than L2 (512 MiB read + 512 MiB written per step); no flush",

@@ -184,14 +184,15 @@ typedef struct {
  * launches ignore it, and launches with prefetch_boxes or poll_suspend_ns set
  * always take the warp consumer.
  *   ATB_CONSUMER_AUTO   the library's choice: the one-thread drain for
- *                       stages of 32 KiB and more, and for stages of 8 to
+ *                       stages of 32 KiB and more, and for stages of 4 to
  *                       32 KiB when the launch leaves stages, store_groups
  *                       and ctas_per_sm at 0 (the drain then runs its own
- *                       ring: about 64 KiB of stages for boxes being loaded
+ *                       ring: 64 KiB of stages per SM for boxes being loaded
  *                       or landed plus 48 KiB of store groups, one CTA per
- *                       SM, each stage freed before the next store is
- *                       issued); the warp consumer otherwise (the faster
- *                       choice for each case on GB300)
+ *                       SM, or below 8 KiB two CTAs with 32 + 16 KiB each;
+ *                       each stage freed before the next store is issued);
+ *                       the warp consumer otherwise (the faster choice for
+ *                       each case on GB300)
  *   ATB_CONSUMER_DRAIN  one consumer thread per CTA waits for each stage and
  *                       issues its drain copy; fewest instructions per box
  *   ATB_CONSUMER_WARP   a consumer warp follows every box and its lane 0

@@ -189,8 +189,12 @@ def test_library_default_launch_shapes(atb):
     s32 = run((256, 64), "none")
     assert (s32["consumer"], s32["release"], s32["stages"], s32["store_groups"], s32["ctas_per_sm"]) == \
         ("drain", "after_store", 3, 2, 1), s32
-    # 4 KiB, or an explicit ring shape below 32 KiB: the warp consumer
-    assert run((64, 32), "128B")["consumer"] == "warp"
+    # 4 KiB: the drain's ring at two CTAs per SM, 8 + 4 stages
+    s4 = run((64, 32), "128B")
+    assert (s4["consumer"], s4["release"], s4["stages"], s4["store_groups"], s4["ctas_per_sm"]) == \
+        ("drain", "before_store", 12, 4, 2), s4
+    # 2 KiB, or an explicit ring shape below 32 KiB: the warp consumer
+    assert run((64, 16), "128B")["consumer"] == "warp"
     assert run((64, 128), "128B", stages=3)["consumer"] == "warp"
     # an explicit order on an explicit ring
     sb = run((64, 128), "128B", consumer="drain", release="before_store", stages=4, store_groups=3, ctas_per_sm=2)
