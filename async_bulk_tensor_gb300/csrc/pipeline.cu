@@ -745,28 +745,15 @@ __device__ void pack_from_wide_s(const PipeArgs& a, uint32_t rb, uint32_t stage,
     const uint32_t first_row = tid / cols;
     if (first_row >= group) return;
     const uint32_t j0 = tid - first_row * cols;
-    constexpr int U = 2;
+    // one row at a time: two rows in flight took the kernel over its register
+    // budget (spills) and measured 13 % slower
     for (uint32_t j = j0; j < cpr; j += cols) {
-        for (uint32_t rho = first_row; rho < rows; rho += U * group) {
-            uint4 A[U], B[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint32_t r = rho + u * group;
-                if (r < rows) {
-                    const uint32_t w = stage + r * a.wide_pitch + 16 * j;
-                    A[u] = ptx::ld_shared_v4_u32(w);
-                    B[u] = ptx::ld_shared_v4_u32(w + 16);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint32_t r = rho + u * group;
-                if (r < rows) {
-                    const uint32_t o = r * row_bytes + 16 * j;
-                    *reinterpret_cast<uint4*>(slot + (o ^ (((o >> 7) & line_mask) << 4))) =
-                        shift_pair<S>(A[u], B[u], bits);
-                }
-            }
+        for (uint32_t r = first_row; r < rows; r += group) {
+            const uint32_t w = stage + r * a.wide_pitch + 16 * j;
+            const uint4 A = ptx::ld_shared_v4_u32(w);
+            const uint4 B = ptx::ld_shared_v4_u32(w + 16);
+            const uint32_t o = r * row_bytes + 16 * j;
+            *reinterpret_cast<uint4*>(slot + (o ^ (((o >> 7) & line_mask) << 4))) = shift_pair<S>(A, B, bits);
         }
     }
 }
