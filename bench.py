@@ -663,9 +663,25 @@ def end_to_end(torch, atb, w, device, stream, src_h, nbytes, bytes_per_step, arg
     atb.check_device(stream)
     ok = bool(torch.equal(out_pin, src_pin))  # the whole host output of the last step
     units, max_s = aggregate(dist, seconds, float(bytes_per_step) * steps, device)
-    return {"value": round(units / max_s / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
+    # the host link this box gives the same buffers: one H2D and one D2H copy of the whole tensor at once, on
+    # two streams, no kernel (the ceiling of any host-buffer round trip of this size)
+    up, down = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    link = []
+    for _ in range(4):
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(up):
+            src.copy_(src_pin, non_blocking=True)
+        with torch.cuda.stream(down):
+            out_pin.copy_(dst, non_blocking=True)
+        torch.cuda.synchronize(device)
+        link.append(2 * nbytes / (time.perf_counter() - t0) / 1e9)
+    link_gbs = max(link[1:])
+    value = units / max_s / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": nbytes, "steps": steps, "ms_per_step": round(max_s / steps * 1e3, 3),
-            "slabs": args.slabs or 12, "call": "atb_tile_roundtrip_host", "verified": ok}
+            "slabs": args.slabs or 12, "call": "atb_tile_roundtrip_host", "verified": ok,
+            "host_link_bidirectional_GBps": round(link_gbs, 1), "frac_of_host_link": round(value / link_gbs, 3)}
 
 
 def cpu_baseline(w, src_h, repeats: int = 4):
