@@ -157,16 +157,20 @@ typedef struct {
 
 /* Pipeline shape of one launch.  Zero fields take the library defaults. */
 typedef struct {
-    uint32_t stages;       /* shared-memory ring depth, 1..16 (0 = 3, or fewer if 3 do not fit;
-                              the drain's own ring: see atb_launch.consumer) */
+    uint32_t stages;       /* shared-memory ring depth, 1..16 (0 = the library's choice: 3, or
+                              fewer if 3 do not fit, but for the consumers' own rings,
+                              see atb_launch.consumer and atb_launch.release) */
     uint32_t ctas;         /* total CTAs; 0 = persistent grid of ctas_per_sm per SM */
-    uint32_t ctas_per_sm;  /* 0 = about 96 KiB of stages per SM (1..8), within what fits;
-                              one for the drain's own ring */
+    uint32_t ctas_per_sm;  /* 0 = the library's choice: about 96 KiB of stages per SM (1..8),
+                              within what fits, but for the consumers' own rings (one or
+                              two per SM) */
     uint32_t schedule;     /* 0 = box t goes to CTA t mod G; 1 = CTA b takes a contiguous run */
     uint32_t store_groups; /* bulk-store groups allowed in flight at once, 1..8, clamped to
-                              `stages` (0 = the library's choice, 2 but for the
-                              drain's own ring); a stage is recycled as soon as
-                              the group that stores from it has finished reading it */
+                              `stages` (0 = the library's choice: 2, but for the consumers'
+                              own rings); a stage is recycled as soon as the group that
+                              stores from it has finished reading it.  Giving any of
+                              stages, ctas_per_sm or store_groups turns the own rings off:
+                              the other two then take the common defaults */
     uint32_t l2_hints;     /* ATB_HINT_* bits: L2 eviction policy of the box loads and stores */
     uint32_t no_pdl;       /* 1 = launch without programmatic dependent launch (see below) */
     uint32_t poll_suspend_ns; /* mbarrier waits: suspend-time hint per poll in ns (0 = hardware default) */
