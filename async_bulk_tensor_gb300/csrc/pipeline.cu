@@ -1721,6 +1721,16 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
         // sized on the box image: a wider stage for off-grid loads does not cut the CTA count
         uint64_t want = kStageBytesPerSm / (static_cast<uint64_t>(stages) * stage_bytes_for(shape));
         want = want < 1 ? 1 : (want > kMaxDefaultCtasPerSm ? kMaxDefaultCtasPerSm : want);
+        // A short launch, whose CTAs would each see no more than four ring-fulls
+        // of boxes, spreads them over as many CTAs per SM as fit, up to one
+        // ring-full each, so that more of its boxes are in flight from the start
+        // (workload 2, 924 boxes of 32 KiB, two CTAs per SM instead of one: 9.3
+        // -> 6.1 us back to back, 13.0 -> 12.5 us after an L2 flush, on GB300).
+        const uint64_t sms = static_cast<uint64_t>(dev.sm_count);
+        if (n_tiles <= 4 * sms * want * stages) {
+            const uint64_t spread = (n_tiles + sms * stages - 1) / (sms * stages);
+            if (spread > want) want = spread > kMaxDefaultCtasPerSm ? kMaxDefaultCtasPerSm : spread;
+        }
         per_sm = static_cast<uint32_t>(fit < 1 ? 1 : (static_cast<uint64_t>(fit) < want ? fit : want));
     }
     uint64_t grid = cfg && cfg->ctas ? cfg->ctas : static_cast<uint64_t>(dev.sm_count) * per_sm;

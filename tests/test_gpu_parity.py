@@ -185,10 +185,11 @@ def test_library_default_launch_shapes(atb):
     # 8 KiB: 8 + 6 stages
     s8 = run((64, 64), "128B")
     assert (s8["consumer"], s8["release"], s8["stages"], s8["store_groups"]) == ("drain", "before_store", 14, 6), s8
-    # 32 KiB: the drain on the common default ring, freeing after the store
+    # 32 KiB: the drain on the common default ring, freeing after the store; 1,024 boxes are a short
+    # launch (under four ring-fulls per CTA at one CTA per SM), spread over two CTAs per SM
     s32 = run((256, 64), "none")
     assert (s32["consumer"], s32["release"], s32["stages"], s32["store_groups"], s32["ctas_per_sm"]) == \
-        ("drain", "after_store", 3, 2, 1), s32
+        ("drain", "after_store", 3, 2, 2), s32
     # 4 KiB: the drain's ring at two CTAs per SM, 8 + 4 stages
     s4 = run((64, 32), "128B")
     assert (s4["consumer"], s4["release"], s4["stages"], s4["store_groups"], s4["ctas_per_sm"]) == \
