@@ -253,6 +253,15 @@ RELEASES = {"auto": 0, "after_store": 1, "before_store": 2}
 
 def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0, l2_hints=0, pdl=True,
             poll_suspend_ns=0, prefetch_boxes=0, checks=0, consumer="auto", release="auto") -> Launch:
+    """The ``atb_launch`` record of every call's keyword options; 0 / "auto" leave a field to the library.
+
+    stages, ctas, ctas_per_sm, store_groups: the ring's shape (giving any of stages, ctas_per_sm or
+    store_groups turns the consumers' own rings off); schedule: "strided" or "contiguous"; l2_hints:
+    ATB_HINT_* bits; pdl: programmatic dependent launch; poll_suspend_ns, prefetch_boxes, checks
+    (CHECK_RING); consumer: "auto", "drain" or "warp" (tile-grid launches); release: "auto",
+    "after_store" or "before_store" (when the drain or the several-warp consumer frees a stage).
+    ``last_launch()`` reports what a call resolved.
+    """
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,
                   store_groups, l2_hints, 0 if pdl else 1, poll_suspend_ns, prefetch_boxes, checks,
                   CONSUMERS[consumer] if isinstance(consumer, str) else consumer,
