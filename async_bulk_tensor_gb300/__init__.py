@@ -259,7 +259,7 @@ def _launch(stages=0, ctas=0, ctas_per_sm=0, schedule="strided", store_groups=0,
     store_groups turns the consumers' own rings off); schedule: "strided" or "contiguous"; l2_hints:
     ATB_HINT_* bits; pdl: programmatic dependent launch; poll_suspend_ns, prefetch_boxes, checks
     (CHECK_RING); consumer: "auto", "drain" or "warp" (tile-grid launches); release: "auto",
-    "after_store" or "before_store" (when the drain or the several-warp consumer frees a stage).
+    "after_store" or "before_store" (when the consumer frees a stage).
     ``last_launch()`` reports what a call resolved.
     """
     return Launch(stages, ctas, ctas_per_sm, SCHEDULES[schedule] if isinstance(schedule, str) else schedule,

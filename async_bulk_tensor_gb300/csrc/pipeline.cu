@@ -1202,7 +1202,11 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
             break;
         }
         const uint32_t t = cur.t;
-        if (lane == 0) ring_check_filled(a, r, s, k, t);
+        if (lane == 0) {
+            ring_check_filled(a, r, s, k, t);
+            if (a.early_release)  // free the stage of every box stored at least store_groups boxes back
+                pending.retire(a, r, k, a.store_lag + 1);
+        }
         int32_t c[R];
         cur.grid_origin(a, c);  // every lane follows the same cursor
         // kLoad: kStoreTensor means "drain the image to the packed buffer"
@@ -1225,7 +1229,7 @@ __global__ void __launch_bounds__(kPipelineThreads, 1)
                 ring_note_freed(a, r, s, k);
                 ptx::mbar_arrive(r.empty(s));  // written by the warp, or nothing to write
             }
-            pending.retire(a, r, k, a.store_lag);
+            if (!a.early_release) pending.retire(a, r, k, a.store_lag);
         }
     }
 
@@ -1683,12 +1687,11 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     if (groups > stages) groups = stages;
     if (groups > 8) groups = 8;
     const uint32_t release = cfg ? cfg->release : ATB_RELEASE_AUTO;
-    const bool releases = drain || wide;  // the consumers that honour atb_launch.release
-    if (releases && release == ATB_RELEASE_BEFORE_STORE && groups >= stages)
+    if (release == ATB_RELEASE_BEFORE_STORE && groups >= stages)
         return set_error(ATB_ERR_ARG, "releasing before the next store needs store_groups (%u) < stages (%u)", groups,
                          stages);
-    const bool early = releases && groups < stages &&
-                       (release == ATB_RELEASE_BEFORE_STORE || (release == ATB_RELEASE_AUTO && (deep || wide_deep)));
+    const bool early =
+        groups < stages && (release == ATB_RELEASE_BEFORE_STORE || (release == ATB_RELEASE_AUTO && (deep || wide_deep)));
     if (n_tiles == 0) return ATB_OK;
 
     DeviceStatus* status = caller_status;
@@ -1813,7 +1816,7 @@ atb_status launch_pipeline(const atb_tensor_map* src, const atb_tensor_map* dst,
     if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     atb_launch_shape& ls = g_last_shape;
     ls.consumer = wide ? ATB_CONSUMER_WARPS : drain ? ATB_CONSUMER_DRAIN : ATB_CONSUMER_WARP;
-    ls.release = !(drain || wide) ? 0u : a.early_release ? ATB_RELEASE_BEFORE_STORE : ATB_RELEASE_AFTER_STORE;
+    ls.release = a.early_release ? ATB_RELEASE_BEFORE_STORE : ATB_RELEASE_AFTER_STORE;
     ls.stages = stages;
     ls.store_groups = groups;
     ls.ctas_per_sm = per_sm;

@@ -208,10 +208,8 @@ typedef struct {
 #define ATB_CONSUMER_WARP  2u
 
 /*
- * atb_launch.release, for launches the one-thread drain or the several-warp
- * consumer (coordinate lists, the fp32 update) serves: when a stage whose box
- * is being stored is handed back to the producer.  The warp consumer ignores
- * it.
+ * atb_launch.release: when a stage whose box is being stored is handed back
+ * to the producer (every consumer).
  *   ATB_RELEASE_AUTO          the library's choice: before the next store on
  *                             the drain's own ring and on the several-warp
  *                             consumer's own ring (16-32 KiB stages, no shape
@@ -353,8 +351,7 @@ atb_status atb_pipeline_smem_bytes(const atb_tensor_map* map, uint32_t stages, s
  *   consumer      ATB_CONSUMER_DRAIN or ATB_CONSUMER_WARP for tile-grid
  *                 launches; ATB_CONSUMER_WARPS for launches with several
  *                 consumer warps (coordinate lists and the fp32 update)
- *   release       the drain's ATB_RELEASE_AFTER_STORE or
- *                 ATB_RELEASE_BEFORE_STORE; 0 for the other consumers
+ *   release       ATB_RELEASE_AFTER_STORE or ATB_RELEASE_BEFORE_STORE
  *   stages, store_groups, ctas_per_sm, ctas (the grid), threads per CTA,
  *   smem_bytes (dynamic shared memory per CTA), boxes (boxes the launch moves)
  * ATB_ERR_ARG if out is NULL.

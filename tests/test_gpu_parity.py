@@ -202,6 +202,8 @@ def test_library_default_launch_shapes(atb):
     assert (sb["release"], sb["stages"], sb["store_groups"], sb["ctas_per_sm"]) == ("before_store", 4, 3, 2), sb
     sa = run((64, 128), "128B", consumer="drain", release="after_store")
     assert (sa["release"], sa["stages"], sa["store_groups"]) == ("after_store", 7, 3), sa
+    sw = run((64, 128), "128B", consumer="warp", release="before_store", stages=4, store_groups=2)
+    assert (sw["consumer"], sw["release"], sw["stages"], sw["store_groups"]) == ("warp", "before_store", 4, 2), sw
     # freeing before the next store needs a stage beyond the store groups
     dst = dev_empty(src_h.size, fill=0)
     ms = atb.encode_tiled("f16", src, dims, strides, (64, 128), "128B")
@@ -326,10 +328,11 @@ def _small_case(name, dtype, dims, box, swizzle, order, seed):
                                     dict(consumer="drain", release="before_store", stages=4, store_groups=2, ctas=3),
                                     dict(consumer="drain", release="before_store", stages=5, store_groups=3, ctas=2,
                                          checks=1, l2_hints=3),
-                                    dict(consumer="drain", release="after_store")],
+                                    dict(consumer="drain", release="after_store"),
+                                    dict(consumer="warp", release="before_store", stages=3, store_groups=2, ctas=4)],
                          ids=["s1c1", "s3c5g2", "s2c3contig", "default", "prefetch3_hints", "ring_check",
                               "ring_check_s2c3g2", "drain", "warp_s2g1", "before_s2g1", "before_s4g2c3",
-                              "before_s5g3c2_check_hints", "drain_after"])
+                              "before_s5g3c2_check_hints", "drain_after", "warp_before_s3g2c4"])
 def test_small_cases_all_ops(atb, case, launch):
     name, dtype, dims, box, swizzle, order = case
     v, src_h, nbytes, coords_h = _small_case(name, dtype, dims, box, swizzle, order, 1000 + len(name))
