@@ -99,7 +99,10 @@ atb_status device_status_block(DeviceStatus** out)
             return cuda_error(e, "cudaMemset(status block)");
         }
         e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) return cuda_error(e, "cudaDeviceSynchronize");
+        if (e != cudaSuccess) {
+            cudaFree(p);
+            return cuda_error(e, "cudaDeviceSynchronize");
+        }
         g_status[info.device] = static_cast<DeviceStatus*>(p);
     }
     *out = g_status[info.device];
