@@ -22,9 +22,10 @@
  *     one-chunk-wider descriptor (map_wide) from the origin rounded down to
  *     the grid, and the kernel's consumer threads cut the box out of that
  *     wider image (or, without map_wide, load it with plain loads); boxes
- *     written to a tensor from such an origin leave through plain stores of
- *     aligned 16-byte chunks.  The result is the same as for any other
- *     origin.  Tile-grid origins are always on the grid.
+ *     written to a tensor from such an origin leave through aligned plain
+ *     stores of 1, 2 or 4 bytes, each wholly inside the box.  The result is
+ *     the same as for any other origin.  Tile-grid origins are always on the
+ *     grid.
  *   - A "packed" buffer holds n box images back to back, image i at byte
  *     offset i * box_bytes, each byte-for-byte the shared-memory image of that
  *     box as the engine writes it (swizzle applied, stage base aligned to the
@@ -47,9 +48,10 @@
  *     sets up its shared memory, and waits for that kernel to complete (with
  *     its memory visible) before it touches global memory.  Stream order is
  *     therefore kept exactly; atb_launch.no_pdl = 1 turns the overlap off.
- *   - Errors raised inside a kernel (a wait that ran out of time, a misaligned
- *     box origin) are recorded in the device status block and reported by
- *     atb_device_status(); the kernel returns early instead of hanging.
+ *   - Errors raised inside a kernel (a wait that ran out of time, a listed
+ *     origin beyond +-2^30) are recorded in the device status block and
+ *     reported by atb_device_status(); the kernel returns early instead of
+ *     hanging.
  *   - Every call may be made from any host thread.  atb_last_error() is
  *     kept per thread: it describes the last failed call of the calling
  *     thread.  Host-resident round trips (atb_tile_roundtrip_host) share
@@ -383,9 +385,10 @@ atb_status atb_last_launch(atb_launch_shape* out);
  * phase and drains the landed image with a 1-D bulk store to
  * d_packed + i * box_bytes, recycling the stage after the bulk group's reads.
  * Calls with a coordinate list run four consumer warps: a listed box whose x
- * origin is off the 16-byte grid is armed with no bytes, and those warps
- * build its image with plain loads (the fill value outside the tensor, the
- * same bytes the engine writes) before it is drained.
+ * origin is off the 16-byte grid is loaded through map_wide from the origin
+ * rounded down to the grid, and those warps cut its image out of the wider
+ * one (without map_wide they build it with plain loads, writing the same
+ * fill bytes as the engine outside the tensor) before it is drained.
  *
  *   src       encoded map of the source tensor
  *   d_coords  device array of n * rank int32 origins, innermost first; NULL =
