@@ -38,6 +38,19 @@ MUTANTS = {
     "add_subtracts": ("x = x + addend;", "x = x - addend;"),
     "roundtrip_skips_store": ("    oracle_tile_store(dst, dst_base, coords, n, packed);\n    free(packed);\n    return 0;\n}\n\n/*",
                               "    free(packed);\n    return 0;\n}\n\n/*"),
+    "grid_drops_ragged_last_tile": ("return (v->dims[d] + v->box[d] - 1) / v->box[d];", "return v->dims[d] / v->box[d];"),
+    "visits_rounded_down": ("return (v->box[d] + step_along(v, d) - 1) / step_along(v, d);",
+                            "return v->box[d] / step_along(v, d);"),
+    "grid_origin_is_tile_index": ("= (int32_t)(t_d * v->box[d]);", "= (int32_t)t_d;"),
+    "address_without_strides": ("addr += (uint64_t)g[d] * v->strides[d];", "addr += (uint64_t)g[d] * (uint64_t)v->esize;"),
+    "load_forgets_fill": ("= inside ? base[addr + (uint64_t)b] : 0;", "= base[addr + (uint64_t)b];"),
+    "packed_slots_by_elements": ("uint8_t* image = packed + i * box_bytes;", "uint8_t* image = packed + i * box_elems;"),
+    "box_index_split_by_extent_not_visits": ("int64_t k = (int64_t)(rest % visits_along(v, d));\n        rest /= visits_along(v, d);",
+                                             "int64_t k = (int64_t)(rest % v->box[d]);\n        rest /= v->box[d];"),
+    "store_in_reverse_list_order": ("for (uint64_t i = 0; i < n; ++i) {\n        const int32_t* c = coords + i * (uint64_t)v->rank;\n        const uint8_t* image",
+                                    "for (uint64_t i = n; i-- > 0;) {\n        const int32_t* c = coords + i * (uint64_t)v->rank;\n        const uint8_t* image"),
+    "update_skipped": ("    oracle_add_f32(packed, n * box_bytes, addend);\n", ""),
+    "update_first_box_only": ("oracle_add_f32(packed, n * box_bytes, addend);", "oracle_add_f32(packed, box_bytes, addend);"),
 }
 
 
