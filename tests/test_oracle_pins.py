@@ -425,6 +425,38 @@ def test_gather_3d_steps_and_swizzle():
         np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], want)
 
 
+def test_gather_4d_steps_on_middle_dimensions_brute_force():
+    # a step on every outer dimension, the two middle ones included; any x origin
+    esize = 2
+    dims, box, steps = (8, 7, 6, 5), (8, 5, 4, 3), (1, 2, 3, 2)
+    strides = (2, 32, 32 * 7 + 16, (32 * 7 + 16) * 6)
+    v = oracle.View(esize, dims, strides, box, "none", steps)
+    assert oracle.box_bytes(v) == 8 * 3 * 2 * 2 * esize  # ceil(5/2), ceil(4/3), ceil(3/2) visits
+    buf = datagen.random_bytes(v.span_bytes() + 16, 94)
+    g = datagen.rng(4)
+    origins = np.stack([g.integers(-7, 8, 60)] + [g.integers(-b, n, 60) for b, n in zip(box[1:], dims[1:])],
+                       1).astype(np.int32)
+    packed = oracle.tile_load(v, buf, origins)
+    bb = oracle.box_bytes(v)
+    for i, o in enumerate(origins):
+        np.testing.assert_array_equal(packed[i * bb:(i + 1) * bb], np_box_stepped(buf, v, o).reshape(-1),
+                                      err_msg=f"origin {o}")
+
+
+def test_store_overlapping_boxes_later_box_wins():
+    # boxes are applied in list order: where two boxes with different images
+    # overlap, the one listed later leaves its bytes
+    v = oracle.View(1, (32, 4), (1, 32), (16, 4))
+    ones, twos = np.full(64, 0x11, np.uint8), np.full(64, 0x22, np.uint8)
+    base = np.zeros(128, dtype=np.uint8)
+    oracle.tile_store(v, base, np.array([[0, 0], [8, 0]], dtype=np.int32), np.concatenate([ones, twos]))
+    rows = base.reshape(4, 32)
+    assert (rows[:, :8] == 0x11).all() and (rows[:, 8:24] == 0x22).all() and (rows[:, 24:] == 0).all()
+    base[:] = 0
+    oracle.tile_store(v, base, np.array([[8, 0], [0, 0]], dtype=np.int32), np.concatenate([twos, ones]))
+    assert (rows[:, :16] == 0x11).all() and (rows[:, 16:24] == 0x22).all() and (rows[:, 24:] == 0).all()
+
+
 def test_store_with_steps_writes_only_visited_elements():
     rows, cols = 17, 32
     v = oracle.View(4, (cols, rows), (4, 128), (32, 8), "none", (1, 3))
