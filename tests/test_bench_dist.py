@@ -86,3 +86,23 @@ def test_bench_rejects_short_warmup():
 
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_traffic_is_reported_only_for_the_kernel_it_was_measured_on(monkeypatch, tmp_path):
+    import hashlib
+
+    import bench
+
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel source\n")
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    profile = tmp_path / "profile.md"
+    profile.write_text(f"    traffic_bytes_per_launch: 1234567\n    kernel_source_sha256_16: {digest}\n")
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", [str(src)])
+    monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(profile))
+    assert bench.committed_traffic()[0] == 1234567
+    src.write_text("// kernel source, changed\n")
+    value, why = bench.committed_traffic()
+    assert value is None and "changed" in why
+    monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(tmp_path / "missing.md"))
+    assert bench.committed_traffic()[0] is None
