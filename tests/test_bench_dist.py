@@ -106,3 +106,21 @@ def test_traffic_is_reported_only_for_the_kernel_it_was_measured_on(monkeypatch,
     assert value is None and "changed" in why
     monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(tmp_path / "missing.md"))
     assert bench.committed_traffic()[0] is None
+
+
+def test_in_bound_bytes_of_workload4_agree_with_the_oracle_fill_mask():
+    # the algorithmic bytes of the workload-4 lines: every box byte the engine
+    # reads rather than fills, counted two independent ways
+    import numpy as np
+
+    import bench
+    import datagen
+    import oracle
+
+    w = datagen.C4
+    coords = datagen.workload_coords(w)
+    v = oracle.View(w.esize, w.dims, w.strides, w.box, w.swizzle)
+    filled = int(oracle.tile_oob_mask(v, coords).astype(np.int64).sum())
+    inb = bench.box_inbound_bytes(w.dims, w.box, w.esize, coords)
+    assert inb == len(coords) * oracle.box_bytes(v) - filled
+    assert inb == 29_045_120  # the figure the workload-4 profiles quote
